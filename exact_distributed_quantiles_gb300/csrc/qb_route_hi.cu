@@ -1,0 +1,11 @@
+// qb_route_hi.cu -- instantiates the fused router pass in mode kModeHi.
+#include "qb_route.cuh"
+
+namespace qb {
+int launch_route_hi(const void* logits, int dtype, const float* bias, int64_t N, int E, int k,
+                    int32_t* hist, uint16_t* keys_out, int32_t* topk_out, float* alpha_out,
+                    const int32_t* sel, const float* bounds, int nbins, cudaStream_t stream) {
+  return route::launch_mode<kModeHi>(logits, dtype, bias, N, E, k, hist, keys_out, topk_out,
+                                alpha_out, sel, bounds, nbins, stream);
+}
+}  // namespace qb

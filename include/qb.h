@@ -1,0 +1,183 @@
+/*
+ * qb.h -- C ABI of libqb: the data-parallel hot path of bias-based quantile
+ * balancing (QB) for Mixture-of-Experts routers, on one NVIDIA GB300 (sm_103a).
+ *
+ * Sources (web pages, cited by title and section):
+ *   [QB-PR] "[Dev] Add global-batch quantile balancing" (Megatron-LM pull
+ *           request 6637).  "Quantile estimator": s[i,j] is the raw sigmoid
+ *           router score, alpha[i] the (k+1)-th largest value of s[i,:] + b,
+ *           r[i,j] = alpha[i] - s[i,j], b_next[j] = quantile(r[:,j], k/E),
+ *           then b_next -= mean(b_next); the K3 histogram spans
+ *           [min(b_next)-1, max(b_next)+1] with 1000 uniform bins per expert.
+ *           "Implementation": one persistent-address int32 histogram
+ *           [num_experts, num_bins] accumulated over every microbatch; bias and
+ *           bounds updated in place once; histogram reset without changing
+ *           its address.
+ *   [EQB]   "Exact Quantile Balancing and Load-Error Injection for Mixture-of-
+ *           Experts".  EQB paragraph: histogram the high byte of the BF16
+ *           margins (256 bins per expert), locate the bin holding the r-th
+ *           smallest value, histogram the low byte within that bin,
+ *           concatenate the bytes.  LEI paragraph: add eta * rho_e to the
+ *           score gradient of expert e for every token of the local batch.
+ *
+ * Conventions common to every entry point
+ *   - Pointers marked "device" are CUDA device pointers; the caller owns every
+ *     buffer.  The library allocates nothing and keeps no host state.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL is the legacy default stream).  Argument errors are detected on the
+ *     host and returned before anything is launched; nothing is written then.
+ *   - Layouts are row-major.  logits / scores / grads are [N, E] with the
+ *     expert index contiguous.  EQB histograms are int32 [E, 256]; K3
+ *     histograms are int32 [E, nbins].
+ *   - Histograms accumulate (+=).  Zero them once before the first microbatch
+ *     of a global batch (qb_zero_i32), or let the finalize call reset them in
+ *     place.  Counts are int32: the pooled token count must stay below 2^31.
+ *   - Inputs must be finite; results on NaN logits are unspecified.
+ *   - Supported expert counts: E in {32, 64, 128, 256, 512}.  Supported k:
+ *     1 <= k <= 15 and k < E.
+ *   - Return value: QB_OK (0) or a negative qb_status.
+ */
+#ifndef QB_H
+#define QB_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QB_OK = 0,
+  QB_EINVAL = -1,        /* null / misaligned pointer, bad size, bad rank  */
+  QB_EUNSUPPORTED = -2,  /* E or k outside the compiled variants           */
+  QB_ECUDA = -3,         /* a CUDA launch or runtime call failed           */
+  QB_EOVERFLOW = -4,     /* a count would not fit its int32 counter        */
+  QB_EDEVICE = -5        /* a kernel reported a device-side error          */
+} qb_status;
+
+typedef enum { QB_F32 = 0, QB_BF16 = 1 } qb_dtype;
+
+/* Human-readable text for a status code (static storage). */
+const char* qb_status_string(int status);
+
+/* Library version string. */
+const char* qb_version(void);
+
+/* Rank of the k/E quantile among n_pool pooled samples, 1-based:
+ * r = ceil(k * n_pool / E) in integer arithmetic.  This is the type-1
+ * (inverse-CDF) reading of "quantile(r[:,j], k/E)" ([QB-PR] "Quantile
+ * estimator") that makes the two-byte radix select of [EQB] return one
+ * element.  Returns a negative qb_status on bad arguments. */
+int64_t qb_rank(int64_t n_pool, int E, int k);
+
+/* Pinned logistic function, element-wise: s[i] = sigma(x[i]) as the fixed
+ * binary32 operation sequence the routing kernels use ([QB-PR] "raw sigmoid
+ * router score").  x, s: device fp32 [n]; may alias. */
+int qb_sigmoid(const float* x, float* s, int64_t n, void* stream);
+
+/* Fill n int32 values with zero (a convenience for histograms). */
+int qb_zero_i32(int32_t* p, int64_t n, void* stream);
+
+/* ---------------------------------------------------------------- EQB ---- */
+
+/* Route one microbatch and accumulate the EQB hi-byte histogram.
+ * ([QB-PR] "Quantile estimator"; [EQB] EQB paragraph, first pass.)
+ *   logits   device [N, E], fp32 (dtype QB_F32) or bf16 (QB_BF16); 16-byte
+ *            aligned.
+ *   bias     device fp32 [E], the selection bias used by this forward pass.
+ *   hist_hi  device int32 [E, 256]; hist_hi[j][key>>8] += 1 for every token,
+ *            where key is the order-preserving key of RN_bf16(r[i,j])
+ *            (-0 folded to +0; key = bits ^ (sign ? 0xFFFF : 0x8000)).
+ *   keys_out optional device uint16 [N, E] (16-byte aligned): the keys, for
+ *            qb_keys_hist_lo.  NULL to skip.
+ *   topk_out optional device int32 [N, k]: the k experts of largest s + b
+ *            (ties to the lower index), ascending expert index.  NULL to skip.
+ *   alpha_out optional device fp32 [N]: alpha per token.  NULL to skip.
+ * Several calls (one per microbatch) accumulate into the same hist_hi. */
+int qb_route_hist_hi(const void* logits, int dtype, const float* bias, int64_t N, int E, int k,
+                     int32_t* hist_hi, uint16_t* keys_out, int32_t* topk_out, float* alpha_out,
+                     void* stream);
+
+/* Select the hi-byte bin that holds the rank-r value of every expert
+ * ([EQB] EQB paragraph: "locate the bin holding the r-th smallest value").
+ *   hist_hi  device int32 [E, 256], pooled over the whole global batch.
+ *   r        1-based rank, from qb_rank(N_pool, E, k).
+ *   sel      device int32 [E]: first bin b with sum_{b'<=b} hist_hi[j][b'] >= r.
+ *   r_lo     device int32 [E]: r minus the count of the bins below sel.
+ * A row holding fewer than r samples yields sel = -1, r_lo = 0. */
+int qb_select_hi(const int32_t* hist_hi, int E, int64_t r, int32_t* sel, int32_t* r_lo,
+                 void* stream);
+
+/* Second pass from stored keys ([EQB] EQB paragraph, "a second pass
+ * histograms the low byte within that bin"):
+ *   hist_lo[j][key & 0xFF] += 1 for every key of expert j with key>>8 == sel[j].
+ *   keys device uint16 [N, E] as written by qb_route_hist_hi; 16-byte aligned.
+ * N may cover any number of microbatches (keys stored contiguously). */
+int qb_keys_hist_lo(const uint16_t* keys, int64_t N, int E, const int32_t* sel,
+                    int32_t* hist_lo, void* stream);
+
+/* Second pass recomputed from the logits (same result as qb_keys_hist_lo on
+ * the keys of the same logits and bias, without storing keys). */
+int qb_route_hist_lo(const void* logits, int dtype, const float* bias, int64_t N, int E, int k,
+                     const int32_t* sel, int32_t* hist_lo, void* stream);
+
+/* Finish the select and update the bias ([EQB] "concatenating the two bytes
+ * recovers the exact global quantile"; [QB-PR] "Quantile estimator",
+ * mean-centering; "Implementation", in-place update and reset):
+ *   lo_j  = first bin l with sum_{l'<=l} hist_lo[j][l'] >= r_lo[j]
+ *   q_j   = fp32 value of the bf16 number whose key is (sel_j << 8) | lo_j
+ *   mu    = (sum_j q_j in fp64, ascending j) / E
+ *   bias_out[j] = RN32(q_j - mu)
+ * bias_out (device fp32 [E]) may alias the bias used for routing.
+ * qkey_out optional device uint16 [E] receives the selected keys.
+ * reset != 0 zeroes hist_hi and hist_lo in place afterwards. */
+int qb_finalize(int32_t* hist_hi, int32_t* hist_lo, const int32_t* sel, const int32_t* r_lo,
+                int E, float* bias_out, uint16_t* qkey_out, int reset, void* stream);
+
+/* ----------------------------------------------------------------- K3 ---- */
+
+/* Route one microbatch and accumulate the K3 uniform histogram
+ * ([QB-PR] "Quantile estimator" and "Implementation"):
+ *   w = RN(hi - lo), scale = RN(nbins / w),
+ *   idx = floor(RN(RN(r - lo) * scale)), clamped to [0, nbins-1],
+ *   hist[j][idx] += 1, with r the fp32 margin.
+ *   bounds device fp32 [2] = {lo, hi}, lo < hi (read on the device).
+ *   hist   device int32 [E, nbins]; 1 <= nbins <= 65536. */
+int k3_route_hist(const void* logits, int dtype, const float* bias, int64_t N, int E, int k,
+                  const float* bounds, int nbins, int32_t* hist, void* stream);
+
+/* K3 quantile, centering and next bounds ([QB-PR] "Quantile estimator"):
+ *   b*  = first bin with cumulative count >= r, before = count below it,
+ *   q_j = (lo + b* * width) + width * ((r - before) / count[b*]) in fp64,
+ *         width = (hi - lo) / nbins;
+ *   bias_out[j] = RN32(q_j - mean_j q_j);
+ *   bounds <- {min_j bias_out - 1, max_j bias_out + 1} (fp32, in place).
+ * reset != 0 zeroes hist afterwards.  bounds and bias_out are device. */
+int k3_finalize(int32_t* hist, int E, int nbins, int64_t r, float* bounds, float* bias_out,
+                int reset, void* stream);
+
+/* ---------------------------------------------------------------- LEI ---- */
+
+/* Load-error injection on a run of local batches ([EQB] LEI paragraph).
+ * The N tokens are split into consecutive local batches of `batch_tokens`
+ * tokens (0 means one batch of N; the last batch may be shorter).  For each
+ * batch with n tokens:
+ *   load_e   = #{(i,t) : topk_idx[i,t] == e},   T = n * k / E
+ *   rho_raw  = (load_e - T) / T,   rho_e = tanh(rho_raw_e) - mean_e tanh(rho_raw)
+ *   grad[i,e] = RN32(grad[i,e] + RN32(eta * rho_e)) for every token i of it.
+ *   grad      device fp32 [N, E], updated in place; 16-byte aligned.
+ *   topk_idx  device int32 [N, k], entries in [0, E).
+ *   workspace device fp32 [num_batches * E] scratch owned by the caller
+ *             (num_batches = ceil(N / batch_tokens)); it receives eta*rho. */
+int lei_inject(float* grad, const int32_t* topk_idx, int64_t N, int E, int k, float eta,
+               int64_t batch_tokens, float* workspace, void* stream);
+
+/* Reads and clears the device status word that kernels set instead of
+ * trapping (bit 0: a bounded wait timed out).  Synchronous; returns QB_OK
+ * when clear, QB_EDEVICE when a flag was set, QB_ECUDA on a CUDA error. */
+int qb_device_status(int* flags_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QB_H */

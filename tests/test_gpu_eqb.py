@@ -1,0 +1,199 @@
+"""GPU parity of the EQB path against the CPU oracle (bit-exact).
+
+"Exact Quantile Balancing and Load-Error Injection for Mixture-of-Experts",
+EQB paragraph (hi-byte histogram, select, lo-byte histogram, exact quantile,
+partition invariance); "[Dev] Add global-batch quantile balancing",
+"Quantile estimator" and "Implementation" (alpha, margins, centering, pooled
+histograms, in-place reset with stable addresses, replay counted once).
+"""
+import numpy as np
+import pytest
+import torch
+
+from exact_distributed_quantiles_gb300 import inputs
+from qb_testlib import assert_route_matches, gpu_route, host_logits, np_u16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def qb():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from exact_distributed_quantiles_gb300 import build
+    build.build()
+    from exact_distributed_quantiles_gb300 import qb as _qb
+    return _qb
+
+
+def _logits(N, E, seed, dtype=torch.float32, std=1.0, off_std=0.5):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    off = torch.randn(E, generator=g, device="cuda") * off_std
+    x = torch.randn(N, E, generator=g, device="cuda") * std + off
+    b = (torch.rand(E, generator=g, device="cuda") * 2 - 1) * 0.1
+    return x.to(dtype).contiguous(), b
+
+
+@pytest.mark.parametrize("E", [32, 64, 128, 256, 512])
+@pytest.mark.parametrize("k", [1, 6, 8, 15])
+def test_route_small_shapes_fp32(qb, orc, E, k):
+    if k >= E:
+        pytest.skip("k must be below E")
+    N = 32 * 7 + 13  # several tiles and a ragged tail
+    x, b = _logits(N, E, seed=E * 100 + k)
+    res = gpu_route(qb, x, b, k)
+    ref = assert_route_matches(orc, res, host_logits(x), b.cpu().numpy(), k)
+    assert np.array_equal(res["hist_hi"], orc.hist_hi(orc.keys(ref["margins"])))
+
+
+@pytest.mark.parametrize("E,k", [(64, 6), (256, 8), (512, 6)])
+@pytest.mark.parametrize("N", [1, 31, 32, 33, 1000])
+def test_route_bf16_and_ragged(qb, orc, E, k, N):
+    x, b = _logits(N, E, seed=N + E, dtype=torch.bfloat16, std=1.5, off_std=0.3)
+    res = gpu_route(qb, x, b, k)
+    ref = assert_route_matches(orc, res, host_logits(x), b.cpu().numpy(), k)
+    assert np.array_equal(res["hist_hi"], orc.hist_hi(orc.keys(ref["margins"])))
+
+
+def test_route_ties(qb, orc):
+    # Exact ties in s + b at and around alpha: equal bias entries, duplicated
+    # logit columns, and whole rows of identical values.
+    E, k, N = 64, 6, 300
+    x, b = _logits(N, E, seed=3)
+    b[1::2] = b[0::2]
+    x[:, 1::2] = x[:, 0::2]
+    x[::7, :] = x[::7, :1]
+    b = b.contiguous()
+    x = x.contiguous()
+    res = gpu_route(qb, x, b, k)
+    assert_route_matches(orc, res, host_logits(x), b.cpu().numpy(), k)
+
+
+def test_route_extreme_logits(qb, orc):
+    # |x| beyond the fast exponent range, subnormal scores, margins that round
+    # to bf16 -0 (folded to the +0 key), saturated scores of exactly 1.
+    E, k, N = 64, 6, 96
+    x, b = _logits(N, E, seed=5)
+    x[0:32] = -100.0 + torch.rand(32, E, device="cuda") * 5.0
+    x[32:48] = 90.0 + torch.rand(16, E, device="cuda") * 20.0
+    x[48:64, ::3] = -120.0
+    b[:] = 0.0
+    res = gpu_route(qb, x.contiguous(), b, k)
+    ref = assert_route_matches(orc, res, host_logits(x), b.cpu().numpy(), k)
+    bits = orc.bf16_rne(ref["margins"])
+    assert np.any(bits == 0x8000), "test should produce bf16 -0 margins"
+
+
+def test_route_margins_outside_shared_window(qb, orc):
+    # Large biases push |r| >= 2, whose hi bytes are counted outside the
+    # shared-memory window (direct global atomics).
+    E, k, N = 256, 6, 500
+    x, b = _logits(N, E, seed=9)
+    b = (torch.linspace(-4.0, 4.0, E, device="cuda")).contiguous()
+    res = gpu_route(qb, x, b, k)
+    ref = assert_route_matches(orc, res, host_logits(x), b.cpu().numpy(), k)
+    h = orc.hist_hi(orc.keys(ref["margins"]))
+    assert np.array_equal(res["hist_hi"], h)
+    inside = np.zeros(256, bool)
+    inside[0x40:0x50] = True
+    inside[0xB0:0xC0] = True
+    assert h[:, ~inside].sum() > 0
+
+
+def _eqb_gpu(qb, mbs, bias, k):
+    E = bias.shape[0]
+    st = qb.EQBState(E, bias.device)
+    n_pool = sum(m.shape[0] for m in mbs)
+    keys = torch.empty(n_pool, E, dtype=torch.int16, device=bias.device)
+    b_out = torch.empty_like(bias)
+    row = 0
+    for m in mbs:
+        qb.qb_route_hist_hi(m, bias, k, st.hist_hi, keys_out=keys[row:row + m.shape[0]])
+        row += m.shape[0]
+    r = qb.rank(n_pool, E, k)
+    qb.qb_select_hi(st.hist_hi, r, st.sel, st.r_lo)
+    qb.qb_keys_hist_lo(keys, st.sel, st.hist_lo)
+    h_hi = st.hist_hi.clone()
+    h_lo = st.hist_lo.clone()
+    qb.qb_finalize(st.hist_hi, st.hist_lo, st.sel, st.r_lo, b_out, qkey_out=st.qkey, reset=True)
+    torch.cuda.synchronize()
+    assert qb.device_status() == 0
+    return dict(hist_hi=h_hi.cpu().numpy(), hist_lo=h_lo.cpu().numpy(), sel=st.sel.cpu().numpy(),
+                r_lo=st.r_lo.cpu().numpy(), qkey=np_u16(st.qkey), bias_out=b_out.cpu().numpy(),
+                keys=keys, state=st)
+
+
+def _check_eqb(res, ref):
+    for key in ("hist_hi", "hist_lo", "sel", "r_lo", "qkey"):
+        assert np.array_equal(res[key], ref[key]), key
+    assert np.array_equal(res["bias_out"].view(np.uint32), ref["bias_out"].view(np.uint32))
+
+
+def test_eqb_tiny_workload(qb, orc):
+    w = inputs.WORKLOADS["eqb_tiny"]
+    bias, mbs = inputs.router_layer(w, inputs.seed_for("eqb_tiny"), device="cuda")
+    res = _eqb_gpu(qb, mbs, bias, w.k)
+    ref = orc.eqb_global_batch([host_logits(m) for m in mbs], bias.cpu().numpy(), w.k)
+    _check_eqb(res, ref)
+    assert res["hist_hi"].sum(axis=1).tolist() == [w.n_pool] * w.E
+
+
+def test_eqb_pooled_workload_and_partition_invariance(qb, orc):
+    w = inputs.WORKLOADS["eqb_pooled"]
+    bias, mbs = inputs.router_layer(w, inputs.seed_for("eqb_pooled"), device="cuda")
+    res = _eqb_gpu(qb, mbs, bias, w.k)
+    ref = orc.eqb_global_batch([host_logits(m) for m in mbs], bias.cpu().numpy(), w.k)
+    _check_eqb(res, ref)
+    allx = torch.cat(mbs)
+    for n_m, n_t in ((2, 65536), (32, 4096), (1, 131072)):
+        parts = [allx[i * n_t:(i + 1) * n_t] for i in range(n_m)]
+        other = _eqb_gpu(qb, parts, bias, w.k)
+        for key in ("hist_hi", "hist_lo", "sel", "r_lo", "qkey", "bias_out"):
+            assert np.array_equal(res[key], other[key]), (n_m, key)
+    # rank-local (per-microbatch) histograms differ before pooling
+    h0 = gpu_route(qb, mbs[0], bias, w.k)["hist_hi"]
+    h1 = gpu_route(qb, mbs[1], bias, w.k)["hist_hi"]
+    assert not np.array_equal(h0, h1)
+
+
+def test_lo_pass_recomputed_from_logits_equals_keys_pass(qb, orc):
+    w = inputs.scaled(inputs.WORKLOADS["eqb_pooled"], n_micro=2, n_tokens=3000)
+    bias, mbs = inputs.router_layer(w, 77, device="cuda")
+    res = _eqb_gpu(qb, mbs, bias, w.k)
+    sel = torch.from_numpy(res["sel"]).cuda()
+    h = torch.zeros(w.E, 256, dtype=torch.int32, device="cuda")
+    for m in mbs:
+        qb.qb_route_hist_lo(m, bias, w.k, sel, h)
+    torch.cuda.synchronize()
+    assert np.array_equal(h.cpu().numpy(), res["hist_lo"])
+
+
+def test_reset_in_place_and_replay_counted_once(qb, orc):
+    w = inputs.scaled(inputs.WORKLOADS["eqb_pooled"], n_micro=2, n_tokens=2048)
+    bias, mbs = inputs.router_layer(w, 78, device="cuda")
+    res = _eqb_gpu(qb, mbs, bias, w.k)
+    st = res["state"]
+    ptrs = (st.hist_hi.data_ptr(), st.hist_lo.data_ptr())
+    assert int(st.hist_hi.abs().sum()) == 0 and int(st.hist_lo.abs().sum()) == 0
+    assert (st.hist_hi.data_ptr(), st.hist_lo.data_ptr()) == ptrs
+    # a microbatch replayed after a reset is counted once
+    qb.qb_route_hist_hi(mbs[0], bias, w.k, st.hist_hi)
+    qb.qb_zero_i32(st.hist_hi)
+    qb.qb_route_hist_hi(mbs[0], bias, w.k, st.hist_hi)
+    torch.cuda.synchronize()
+    once = gpu_route(qb, mbs[0], bias, w.k)["hist_hi"]
+    assert np.array_equal(st.hist_hi.cpu().numpy(), once)
+
+
+def test_full_step_layer_at_bench_size(qb, orc):
+    # One layer of the full-step workload in the launch configuration the
+    # benchmark times (all 16 microbatches of the layer in one hi-pass call),
+    # compared with the oracle over every token.
+    w = inputs.WORKLOADS["full_step"]
+    out = torch.empty(w.n_pool, w.E, dtype=torch.float32, device="cuda")
+    bias, mbs = inputs.router_layer(w, inputs.seed_for("full_step", 0), device="cuda", out=out)
+    res = _eqb_gpu(qb, [out], bias, w.k)
+    ref = orc.eqb_global_batch([out.cpu().numpy()], bias.cpu().numpy(), w.k)
+    _check_eqb(res, ref)
+    assert np.array_equal(np_u16(res["keys"]), np.concatenate(ref["keys"]))

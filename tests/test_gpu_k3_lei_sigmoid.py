@@ -1,0 +1,162 @@
+"""GPU parity of the K3 histogram path, LEI and the pinned logistic function.
+
+K3: "[Dev] Add global-batch quantile balancing", "Quantile estimator" and
+"Implementation" -- counts exact, biases within 1e-6 relative to the bias
+vector's scale (bit equality expected: both sides run the same fp64 steps).
+LEI: "Exact Quantile Balancing and Load-Error Injection for Mixture-of-
+Experts", LEI paragraph -- gradients within 1e-6 absolute.
+Sigmoid: the score function, bit-equal to the oracle over all 2^32 inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+from exact_distributed_quantiles_gb300 import inputs
+from qb_testlib import host_logits
+
+pytestmark = pytest.mark.gpu
+
+K3_REL_TOL = 1e-6
+LEI_ABS_TOL = 1e-6
+
+
+@pytest.fixture(scope="module")
+def qb():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from exact_distributed_quantiles_gb300 import build
+    build.build()
+    from exact_distributed_quantiles_gb300 import qb as _qb
+    return _qb
+
+
+# ------------------------------------------------------------------ sigmoid
+
+def test_sigmoid_bit_equal_on_every_binary32_input(qb, orc):
+    chunk = 1 << 28
+    x = torch.empty(chunk, dtype=torch.float32, device="cuda")
+    s = torch.empty_like(x)
+    base = torch.arange(chunk, dtype=torch.int64, device="cuda")
+    mism = 0
+    for c in range(1 << 4):
+        bits = (base + c * chunk).to(torch.int64)
+        bits = torch.where(bits >= (1 << 31), bits - (1 << 32), bits).to(torch.int32)
+        x.copy_(bits.view(torch.float32))
+        qb.qb_sigmoid(x, s)
+        xs = x.cpu().numpy()
+        got = s.cpu().numpy().view(np.uint32)
+        want = orc.sigmoid(xs).view(np.uint32)
+        fin = ~np.isnan(xs)
+        mism += int(np.count_nonzero(got[fin] != want[fin]))
+    assert mism == 0
+
+
+# ------------------------------------------------------------------ K3
+
+def _k3_gpu(qb, mbs, bias, k, bounds0, nbins):
+    E = bias.shape[0]
+    hist = torch.zeros(E, nbins, dtype=torch.int32, device="cuda")
+    bounds = bounds0.clone().cuda()
+    for m in mbs:
+        qb.k3_route_hist(m, bias, k, bounds, hist)
+    n_pool = sum(m.shape[0] for m in mbs)
+    h = hist.clone()
+    b_out = torch.empty_like(bias)
+    qb.k3_finalize(hist, qb.rank(n_pool, E, k), bounds, b_out, reset=True)
+    torch.cuda.synchronize()
+    assert int(hist.abs().sum()) == 0
+    return h.cpu().numpy(), b_out.cpu().numpy(), bounds.cpu().numpy()
+
+
+def _check_k3(res, ref):
+    h, b, bounds = res
+    assert np.array_equal(h, ref["hist"])
+    scale = np.abs(ref["bias_out"]).max()
+    assert np.max(np.abs(b.astype(np.float64) - ref["bias_out"])) <= K3_REL_TOL * scale
+    assert np.allclose(bounds, ref["bounds_out"], rtol=0, atol=K3_REL_TOL * scale)
+    # the same fp64 steps on both sides: expect identical bits
+    assert np.array_equal(b.view(np.uint32), ref["bias_out"].view(np.uint32))
+
+
+def test_k3_workload(qb, orc):
+    w = inputs.WORKLOADS["k3"]
+    bias, mbs = inputs.router_layer(w, inputs.seed_for("k3"), device="cuda")
+    b0 = inputs.k3_initial_bounds(bias)
+    res = _k3_gpu(qb, mbs, bias, w.k, b0, w.nbins)
+    ref = orc.k3_global_batch([host_logits(m) for m in mbs], bias.cpu().numpy(), w.k,
+                              b0.numpy(), w.nbins)
+    _check_k3(res, ref)
+
+
+@pytest.mark.parametrize("E,k,nbins,dtype", [(64, 6, 1000, torch.float32),
+                                              (256, 8, 37, torch.bfloat16),
+                                              (512, 15, 4096, torch.float32)])
+def test_k3_small_shapes(qb, orc, E, k, nbins, dtype):
+    w = inputs.scaled(inputs.WORKLOADS["k3"], E=E, k=k, n_micro=3, n_tokens=32 * 5 + 3,
+                      nbins=nbins, logits_dtype=dtype)
+    bias, mbs = inputs.router_layer(w, 31 + E, device="cuda")
+    b0 = inputs.k3_initial_bounds(bias)
+    res = _k3_gpu(qb, mbs, bias, w.k, b0, nbins)
+    ref = orc.k3_global_batch([host_logits(m) for m in mbs], bias.cpu().numpy(), w.k,
+                              b0.numpy(), nbins)
+    _check_k3(res, ref)
+
+
+def test_k3_out_of_range_clamps(qb, orc):
+    # Narrow bounds that most margins fall outside: clamping to the edge bins.
+    w = inputs.scaled(inputs.WORKLOADS["k3"], E=64, k=6, n_micro=1, n_tokens=500)
+    bias, mbs = inputs.router_layer(w, 5, device="cuda")
+    b0 = torch.tensor([-0.05, 0.05], dtype=torch.float32)
+    res = _k3_gpu(qb, mbs, bias, w.k, b0, 100)
+    ref = orc.k3_global_batch([host_logits(m) for m in mbs], bias.cpu().numpy(), w.k,
+                              b0.numpy(), 100)
+    assert ref["hist"][:, 0].sum() > 0 and ref["hist"][:, -1].sum() > 0
+    _check_k3(res, ref)
+
+
+# ------------------------------------------------------------------ LEI
+
+def test_lei_full_step_microbatches(qb, orc):
+    # Two local batches of the full-step workload: top-6 from the GPU hi pass
+    # with the pre-update bias, eta = 8e-5, grad ~ N(0, 1e-3).
+    w = inputs.scaled(inputs.WORKLOADS["full_step"], n_micro=2)
+    out = torch.empty(w.n_pool, w.E, dtype=torch.float32, device="cuda")
+    bias, _ = inputs.router_layer(w, inputs.seed_for("full_step", 1), device="cuda", out=out)
+    topk = torch.empty(w.n_pool, w.k, dtype=torch.int32, device="cuda")
+    hist = torch.zeros(w.E, 256, dtype=torch.int32, device="cuda")
+    qb.qb_route_hist_hi(out, bias, w.k, hist, topk_out=topk)
+    grad = inputs.score_grad(w, seed=1, n_tokens=w.n_pool, device="cuda")
+    g0 = grad.cpu().numpy()
+    ws = torch.empty(w.n_micro, w.E, dtype=torch.float32, device="cuda")
+    qb.lei_inject(grad, topk, w.eta, ws, batch_tokens=w.n_tokens)
+    torch.cuda.synchronize()
+    t = topk.cpu().numpy()
+    got = grad.cpu().numpy()
+    for m in range(w.n_micro):
+        sl = slice(m * w.n_tokens, (m + 1) * w.n_tokens)
+        want, load, rho = orc.lei(g0[sl], t[sl], w.eta)
+        assert load.sum() == w.n_tokens * w.k
+        assert np.max(np.abs(got[sl] - want)) <= LEI_ABS_TOL
+        c = ws[m].cpu().numpy()
+        assert np.max(np.abs(c - (np.float32(w.eta) * rho).astype(np.float32))) <= 1e-12
+
+
+@pytest.mark.parametrize("N,E,k,bt", [(1, 32, 1, 0), (1000, 64, 6, 333), (4097, 512, 15, 1024)])
+def test_lei_shapes_and_ragged_batches(qb, orc, N, E, k, bt):
+    topk = inputs.random_topk(N, E, k, seed=N, device="cuda")
+    topk[: N // 3] = torch.arange(k, dtype=torch.int32, device="cuda")  # imbalance
+    g = torch.Generator(device="cuda")
+    g.manual_seed(N)
+    grad = torch.randn(N, E, generator=g, device="cuda") * 1e-3
+    g0 = grad.cpu().numpy()
+    bt_eff = bt or N
+    nb = (N + bt_eff - 1) // bt_eff
+    ws = torch.empty(nb, E, dtype=torch.float32, device="cuda")
+    qb.lei_inject(grad, topk, 0.5, ws, batch_tokens=bt)
+    torch.cuda.synchronize()
+    t = topk.cpu().numpy()
+    got = grad.cpu().numpy()
+    for m in range(nb):
+        sl = slice(m * bt_eff, min(N, (m + 1) * bt_eff))
+        want, _, _ = orc.lei(g0[sl], t[sl], 0.5)
+        assert np.max(np.abs(got[sl] - want)) <= LEI_ABS_TOL

@@ -21,7 +21,8 @@ QB_F32, QB_BF16 = 0, 1
 
 EXPORTS = ("qb_status_string", "qb_version", "qb_rank", "qb_sigmoid", "qb_zero_i32",
            "qb_route_hist_hi", "qb_select_hi", "qb_keys_hist_lo", "qb_route_hist_lo",
-           "qb_finalize", "k3_route_hist", "k3_finalize", "lei_inject", "qb_device_status")
+           "qb_finalize", "k3_route_hist", "k3_finalize", "lei_inject", "qb_device_status",
+           "lei_inject_noalloc")
 
 
 class QBError(RuntimeError):
@@ -51,6 +52,7 @@ def _load():
         "k3_finalize": (I, [P, I, I, I64, P, P, I, P]),
         "lei_inject": (I, [P, P, I64, I, I, F, I64, P, P]),
         "qb_device_status": (I, [ctypes.POINTER(ctypes.c_int)]),
+        "lei_inject_noalloc": (I, [P, P, I64, I, I, F, I64, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -169,6 +171,16 @@ def lei_inject(grad, topk_idx, eta, workspace, batch_tokens=0, stream=None):
     _check("lei_inject",
            lib.lei_inject(_ptr(grad), _ptr(topk_idx), N, E, int(k), float(eta), int(batch_tokens),
                           _ptr(workspace), _stream(stream)))
+
+
+def lei_inject_noalloc(grad, topk_idx, eta, batch_tokens=0, stream=None):
+    """lei_inject with the library's own fixed scratch instead of a caller
+    workspace (for callers that cannot allocate device memory)."""
+    N, E = grad.shape
+    k = topk_idx.shape[1]
+    _check("lei_inject_noalloc",
+           lib.lei_inject_noalloc(_ptr(grad), _ptr(topk_idx), N, E, int(k), float(eta),
+                                  int(batch_tokens), _stream(stream)))
 
 
 def device_status() -> int:

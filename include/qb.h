@@ -172,6 +172,26 @@ int k3_finalize(int32_t* hist, int E, int nbins, int64_t r, float* bounds, float
 int lei_inject(float* grad, const int32_t* topk_idx, int64_t N, int E, int k, float eta,
                int64_t batch_tokens, float* workspace, void* stream);
 
+/* Load-error injection without a caller workspace.  The pages have no
+ * counterpart to this entry point; it exists for callers that cannot allocate
+ * device memory where LEI is applied -- code under a framework whose caching
+ * allocator owns the memory pool, services with a device-memory budget fixed
+ * at start-up, or call sites that hold no allocator.
+ * Same arguments and results as lei_inject, minus `workspace`: the eta*rho
+ * scratch lives in a fixed array inside the library's device memory
+ * (65536 floats = 256 KiB per GPU that loads the library, held until process
+ * exit).  Requires ceil(N / batch_tokens) * E <= 65536, else returns
+ * QB_EINVAL before launching anything.  Allocates nothing (no cudaMalloc or
+ * cudaFree).  The first call on a device looks up the array's device address
+ * on that device (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  All calls share the one array, which keeps the last call's
+ * contents (every value read is first written by the same call, so nothing
+ * needs clearing); calls that overlap on the GPU -- on different streams, or
+ * from different host threads -- race on it and must be serialised by the
+ * caller. */
+int lei_inject_noalloc(float* grad, const int32_t* topk_idx, int64_t N, int E, int k, float eta,
+                       int64_t batch_tokens, void* stream);
+
 /* Reads and clears the device status word that kernels set instead of
  * trapping (bit 0: a bounded wait timed out).  Synchronous; returns QB_OK
  * when clear, QB_EDEVICE when a flag was set, QB_ECUDA on a CUDA error. */

@@ -30,47 +30,139 @@ enum : int {
 // One fixed sequence of IEEE-754 binary32 operations (round to nearest even,
 // no flush to zero), so that every score -- and with it every margin and
 // every histogram count -- is reproducible bit for bit:
-//   a = min(|x|, 104);  z = -a
-//   t = fma(z, log2e, 1.5*2^23);  n = t - 1.5*2^23        (n = rint(z*log2e))
-//   u = fma(n, -ln2_hi, z);  u = fma(n, -ln2_lo, u)       (Cody & Waite 1980)
-//   p = degree-7 Taylor polynomial of exp(u), Horner form with fma,
-//       coefficients RN(1/i!)
-//   e = RN(p * 2^n)           (exact exponent add; one rounding if subnormal)
-//   s = RN(num / RN(1 + e)),  num = 1 for x >= 0, e otherwise.
+//   x = clamp(x, -104, 104)
+//   t = fma(x, -log2e, 1.5*2^23);  n = t - 1.5*2^23       (n = rint(-x*log2e))
+//   w = fma(n, ln2_hi, x);  w = fma(n, ln2_lo, w)         (Cody & Waite 1980;
+//                                                          w = x + n*ln2)
+//   p = sum_{i<=7} (-w)^i/i!, Horner in w with fma, coefficients RN((-1)^i/i!)
+//   e = RN(p * 2^n)                      (+inf on overflow)
+//   s = RN(1 / RN(1 + e))                (correctly rounded reciprocal)
+// so s = 1/(1+exp(-x)).  Two implementations of the same function follow:
+// a packed fast path for |x| <= 86 (no over/underflow in the scaling) and an
+// exact scalar path for any input.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float exp_neg_abs(float x) {
-  constexpr float kL2E = 0x1.715476p+0f;
-  constexpr float kMagic = 0x1.8p+23f;
-  constexpr float kLn2Hi = 0x1.62e4p-1f;
-  constexpr float kLn2Lo = 0x1.7f7d1cp-20f;
-  float a = fabsf(x);
-  a = a > 104.0f ? 104.0f : a;
-  const float z = -a;
-  const float t = __fmaf_rn(z, kL2E, kMagic);
-  const float n = __fsub_rn(t, kMagic);
-  float u = __fmaf_rn(n, -kLn2Hi, z);
-  u = __fmaf_rn(n, -kLn2Lo, u);
-  float p = 0x1.a01a02p-13f;          // 1/7!
-  p = __fmaf_rn(p, u, 0x1.6c16c2p-10f);  // 1/6!
-  p = __fmaf_rn(p, u, 0x1.111112p-7f);   // 1/5!
-  p = __fmaf_rn(p, u, 0x1.555556p-5f);   // 1/4!
-  p = __fmaf_rn(p, u, 0x1.555556p-3f);   // 1/3!
-  p = __fmaf_rn(p, u, 0x1.0p-1f);        // 1/2!
-  p = __fmaf_rn(p, u, 1.0f);             // 1/1!
-  p = __fmaf_rn(p, u, 1.0f);             // 1/0!
-  const int ni = __float2int_rz(n);   // exact: n is an integer in [-151, 0]
-  if (ni >= -125) return __int_as_float(__float_as_int(p) + (ni << 23));
-  // Result may be subnormal: scale exactly into the normal range, then apply
-  // the remaining power of two with one correctly rounded multiply.
-  const float q = __int_as_float(__float_as_int(p) + ((ni + 64) << 23));
-  return __fmul_rn(q, 0x1.0p-64f);
-}
+constexpr float kL2E = 0x1.715476p+0f;
+constexpr float kMagic = 0x1.8p+23f;
+constexpr float kLn2Hi = 0x1.62e4p-1f;
+constexpr float kLn2Lo = 0x1.7f7d1cp-20f;
+constexpr float kC0 = 0x1.0p+0f, kC1 = -0x1.0p+0f, kC2 = 0x1.0p-1f, kC3 = -0x1.555556p-3f,
+                kC4 = 0x1.555556p-5f, kC5 = -0x1.111112p-7f, kC6 = 0x1.6c16c2p-10f,
+                kC7 = -0x1.a01a02p-13f;
+constexpr float kFastAbsX = 86.0f;  // |x| <= this: 2^n stays normal, p*2^n exact
+// |x| <= this: every score is above 2^-100, so no margin can round to bf16 -0
+constexpr float kFoldAbsX = 75.0f;
 
 __device__ __forceinline__ float sigmoid_pinned(float x) {
-  const float e = exp_neg_abs(x);
-  const float d = __fadd_rn(1.0f, e);
-  const float num = (x >= 0.0f) ? 1.0f : e;
-  return __fdiv_rn(num, d);
+  float xc = x > 104.0f ? 104.0f : x;
+  xc = xc < -104.0f ? -104.0f : xc;
+  const float t = __fmaf_rn(xc, -kL2E, kMagic);
+  const float n = __fsub_rn(t, kMagic);
+  float w = __fmaf_rn(n, kLn2Hi, xc);
+  w = __fmaf_rn(n, kLn2Lo, w);
+  float p = kC7;
+  p = __fmaf_rn(p, w, kC6);
+  p = __fmaf_rn(p, w, kC5);
+  p = __fmaf_rn(p, w, kC4);
+  p = __fmaf_rn(p, w, kC3);
+  p = __fmaf_rn(p, w, kC2);
+  p = __fmaf_rn(p, w, kC1);
+  p = __fmaf_rn(p, w, kC0);
+  const int ni = __float2int_rz(n);  // exact: n is an integer in [-151, 151]
+  float e;
+  if (ni >= -125 && ni <= 126) {
+    e = __int_as_float(__float_as_int(p) + (ni << 23));
+  } else if (ni > 126) {  // exact scale into range, then one rounding (may overflow)
+    e = __fmul_rn(__int_as_float(__float_as_int(p) + ((ni - 64) << 23)), 0x1.0p+64f);
+  } else {  // may be subnormal: one rounding
+    e = __fmul_rn(__int_as_float(__float_as_int(p) + ((ni + 64) << 23)), 0x1.0p-64f);
+  }
+  return __frcp_rn(__fadd_rn(1.0f, e));
+}
+
+// ---- packed binary32 pairs (sm_100+ f32x2 instructions; same IEEE results
+// as the scalar operations, two lanes per instruction)
+typedef unsigned long long f2_t;
+
+__device__ __forceinline__ f2_t f2_pack(float lo, float hi) {
+  f2_t r;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(f2_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c) {
+  f2_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
+  f2_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2_t f2_sub(f2_t a, f2_t b) {
+  f2_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2_t f2_splat(float v) { return f2_pack(v, v); }
+
+__device__ __forceinline__ float rcp_approx(float d) {
+  float y;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(d));
+  return y;
+}
+
+// Pinned sigmoid of two inputs with |x| <= kFastAbsX.  The reciprocal is
+// RN(1/d) from a hardware estimate refined by two Newton steps
+// y <- y + y*(1 - d*y) in fma form (Markstein's method); equality with the
+// correctly rounded reciprocal is verified on every binary32 input.
+__device__ __forceinline__ f2_t sigmoid2_fast(f2_t X) {
+  const f2_t T = f2_fma(X, f2_splat(-kL2E), f2_splat(kMagic));
+  const f2_t N = f2_sub(T, f2_splat(kMagic));
+  f2_t W = f2_fma(N, f2_splat(kLn2Hi), X);
+  W = f2_fma(N, f2_splat(kLn2Lo), W);
+  f2_t P = f2_fma(f2_splat(kC7), W, f2_splat(kC6));
+  P = f2_fma(P, W, f2_splat(kC5));
+  P = f2_fma(P, W, f2_splat(kC4));
+  P = f2_fma(P, W, f2_splat(kC3));
+  P = f2_fma(P, W, f2_splat(kC2));
+  P = f2_fma(P, W, f2_splat(kC1));
+  P = f2_fma(P, W, f2_splat(kC0));
+  float p0, p1, t0, t1;
+  f2_unpack(P, p0, p1);
+  f2_unpack(T, t0, t1);
+  // t = 1.5*2^23 + n, and (bits(1.5*2^23) << 23) == 0 mod 2^32, so
+  // (bits(t) << 23) == n << 23: adding it to p's exponent multiplies by 2^n.
+  const float e0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
+  const float e1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
+  const f2_t D = f2_add(f2_pack(e0, e1), f2_splat(1.0f));
+  const f2_t ND = f2_sub(f2_splat(0.0f), D);
+  float d0, d1;
+  f2_unpack(D, d0, d1);
+  f2_t Y = f2_pack(rcp_approx(d0), rcp_approx(d1));
+  f2_t R = f2_fma(ND, Y, f2_splat(1.0f));
+  Y = f2_fma(R, Y, Y);
+  R = f2_fma(ND, Y, f2_splat(1.0f));
+  Y = f2_fma(R, Y, Y);
+  return Y;
+}
+
+// Eight inputs in registers -> eight scores; the fast path when all |x| are
+// small enough, the exact scalar path otherwise.  Returns max |x|.
+__device__ __forceinline__ float sigmoid8(const float (&x)[8], float (&s)[8]) {
+  float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+  m = fmaxf(m, fmaxf(fmaxf(fabsf(x[4]), fabsf(x[5])), fmaxf(fabsf(x[6]), fabsf(x[7]))));
+  if (m <= kFastAbsX) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f2_unpack(sigmoid2_fast(f2_pack(x[2 * i], x[2 * i + 1])),
+                                          s[2 * i], s[2 * i + 1]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s[i] = sigmoid_pinned(x[i]);
+  }
+  return m;
 }
 
 // ---------------------------------------------------------------------------

@@ -293,9 +293,21 @@ __global__ void zero_i32_kernel(int32_t* __restrict__ p, int64_t n) {
   }
 }
 
+// The pinned sigmoid through the same code the routing kernels run: chunks
+// of 8 go through sigmoid8 (packed fast path when every |x| <= 86, the exact
+// scalar path otherwise); a tail shorter than 8 uses the scalar path.
 __global__ void sigmoid_kernel(const float* __restrict__ x, float* __restrict__ s, int64_t n) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+  const int64_t n8 = n / 8;
+  for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < n8; c += stride) {
+    float xv[8], sv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) xv[i] = x[8 * c + i];
+    sigmoid8(xv, sv);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s[8 * c + i] = sv[i];
+  }
+  for (int64_t i = 8 * n8 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
     s[i] = sigmoid_pinned(x[i]);
 }
 
@@ -375,7 +387,7 @@ int launch_k3_finalize(int32_t* hist, int E, int nbins, int64_t r, float* bounds
 
 int launch_sigmoid(const float* x, float* s, int64_t n, cudaStream_t stream) {
   if (n <= 0) return QB_OK;
-  int64_t grid = (n + 255) / 256;
+  int64_t grid = (n / 8 + 255) / 256 + 1;
   const int64_t gmax = (int64_t)sm_count() * 16;
   if (grid > gmax) grid = gmax;
   sigmoid_kernel<<<(unsigned)grid, 256, 0, stream>>>(x, s, n);

@@ -13,21 +13,24 @@
 //   inside the selected bin.
 //
 // Work decomposition (one CTA per SM, NW warps, each warp independent):
-//   a warp owns a tile of 32 consecutive tokens held in shared memory,
+//   a warp owns a tile of TILE consecutive tokens held in shared memory,
 //   filled by cp.async.bulk (one mbarrier per warp);
-//   phase A  element-wise over the tile: s = sigma(x) written back in place,
-//            v = s + b, the max of every group of 8 experts;
+//   phase A  element-wise over the tile, 8 experts per lane: s = sigma(x)
+//            (packed f32x2 arithmetic) written back in place, v = s + b, the
+//            max of every group of 8 experts;
 //   phase B  one lane per token: the (k+1)-th largest group max is a lower
 //            bound tau of alpha; only groups whose max reaches tau can hold
 //            any of the k+1 largest v, so alpha is the (k+1)-th largest v of
 //            those groups (a register insertion network);
-//   phase C  element-wise: r = alpha - s, key of RN_bf16(r), keys out,
-//            histogram increments; rows freed here are refilled at once with
-//            the warp's next tile.
+//   phase C  element-wise: r = alpha - s, packed BF16 conversion, key map,
+//            keys out, histogram increments; rows freed here are refilled at
+//            once with the warp's next tile.
 // EQB hi histograms are privatised per CTA for the 32 hi-byte bins that hold
-// margins with 2^-30 <= |r| < 2 (key hi byte 0x40-0x4F and 0xB0-0xBF); other
-// bins go straight to the global histogram.  The shared copy is flushed with
-// one atomic add per non-zero counter when the CTA finishes.
+// margins with 2^-30 <= |r| < 2 (key hi byte 0x40-0x4F and 0xB0-0xBF); a
+// 256-entry table maps a hi byte to its slot, every other byte to a dummy
+// slot that is never flushed, and a warp vote sends the rare steps that saw
+// such a byte through a second loop of direct global atomics.  The shared
+// copy is flushed with one atomic add per non-zero counter per CTA.
 #pragma once
 #include <cuda_bf16.h>
 
@@ -37,8 +40,8 @@
 namespace qb {
 namespace route {
 
-constexpr int kTile = 32;  // tokens per warp tile
-constexpr int kWin = 32;   // hi-byte bins privatised in shared memory
+constexpr int kWin = 32;      // hi-byte bins privatised in shared memory
+constexpr int kDummy = kWin;  // slot of every other bin (never flushed)
 constexpr int kSmemLimit = 227 * 1024;
 
 struct Args {
@@ -50,26 +53,26 @@ struct Args {
   uint16_t* keys_out;
   int32_t* topk_out;
   float* alpha_out;
-  const int32_t* sel;    // lo mode
-  const float* bounds;   // k3 mode
-  int nbins;             // k3 mode
+  const int32_t* sel;   // lo mode
+  const float* bounds;  // k3 mode
+  int nbins;            // k3 mode
   int* status;
 };
 
-template <int E>
+template <int E, int TILE>
 struct Geo {
   static constexpr int G = E / 8;                                   // groups of 8 experts
   static constexpr int GP = ((G / 4 + 1) % 2 == 1) ? G + 4 : G + 8;  // padded gmax row (words)
   static constexpr int LPR = E >= 256 ? 32 : E / 8;                 // lanes per row in a step
   static constexpr int NCOPY = E >= 256 ? 1 : 256 / E;              // histogram copies
-  static constexpr int CSTRIDE = kWin * E + (NCOPY > 1 ? LPR : 0);  // words per copy
-  static constexpr int STEPS = kTile * E / 256;                     // 256-element steps per tile
+  static constexpr int NSLOT = kWin + 1;                            // + dummy slot
+  static constexpr int CSTRIDE = NSLOT * E + (NCOPY > 1 ? LPR : 0);  // words per copy
+  static constexpr int STEPS = TILE * E / 256;                      // 256-element steps per tile
   static constexpr int BREG = E == 512 ? 16 : 8;                    // per-lane bias registers
   // Position of expert e inside one histogram slot row: for a fixed element
-  // index t the 32 lanes of a step land in 32 distinct banks.
-  __device__ static __forceinline__ int pi(int e) {
-    if (E == 512) return (e >> 8) * 256 + (e & 7) * 32 + ((e & 255) >> 3);
-    return (e & 7) * LPR + (e >> 3);
+  // index the 32 lanes of a step land in 32 distinct banks.
+  __host__ __device__ static constexpr int pi(int e) {
+    return E == 512 ? (e >> 8) * 256 + (e & 7) * 32 + ((e & 255) >> 3) : (e & 7) * LPR + (e >> 3);
   }
   __device__ static __forceinline__ int pi_inv(int p) {
     if (E == 512) {
@@ -82,22 +85,22 @@ struct Geo {
 
 __host__ __device__ constexpr int round16(int b) { return (b + 15) & ~15; }
 
-template <int E, typename T, int MODE>
+template <int E, typename T, int MODE, int TILE>
 struct Smem {
-  using GE = Geo<E>;
-  static constexpr int kHist = MODE == kModeHi ? GE::NCOPY * GE::CSTRIDE * 4 : 0;
-  static constexpr int kBias = E * 4;
-  static constexpr int kFixed = kHist + kBias;
-  static constexpr int kTileBytes = kTile * E * 4;  // fp32 scores; bf16 input sits in the upper half
-  static constexpr int kGmax = round16(kTile * GE::GP * 4);
-  static constexpr int kAlpha = round16(kTile * 4);
+  using GE = Geo<E, TILE>;
+  static constexpr int kHist = MODE == kModeHi ? round16(GE::NCOPY * GE::CSTRIDE * 4) : 0;
+  static constexpr int kStatic = 256 + E * 4 + 1024;  // static lut + bias, and a margin
+  static constexpr int kFixed = kHist + kStatic;
+  static constexpr int kTileBytes = TILE * E * 4;  // fp32 scores; bf16 input sits in the upper half
+  static constexpr int kGmax = round16(TILE * GE::GP * 4);
+  static constexpr int kAlpha = round16(TILE * 4);
   static constexpr int kWarp = kTileBytes + kGmax + kAlpha + 16;  // + mbarrier
   static constexpr int nw_fit() {
     int n = (kSmemLimit - kFixed) / kWarp;
     return n > 16 ? 16 : n;
   }
   static constexpr int NW = nw_fit();
-  static constexpr int kTotal = kFixed + NW * kWarp;
+  static constexpr int kTotal = kHist + NW * kWarp;  // dynamic shared memory
 };
 
 // Insert v into the descending list L[0..KMAX) (drops the smallest).
@@ -111,55 +114,60 @@ __device__ __forceinline__ void insert_desc(float (&L)[KMAX], float v) {
   }
 }
 
-template <int KMAX>
+// L[k] for a runtime k < KMAX; a compile-time index when KMAX == k + 1.
+template <int KMAX, bool EXACT>
 __device__ __forceinline__ float pick(const float (&L)[KMAX], int k) {
-  float a = L[0];
+  if constexpr (EXACT) {
+    return L[KMAX - 1];
+  } else {
+    float a = L[0];
 #pragma unroll
-  for (int t = 1; t < KMAX; ++t) a = (t == k) ? L[t] : a;
-  return a;
+    for (int t = 1; t < KMAX; ++t) a = (t == k) ? L[t] : a;
+    return a;
+  }
 }
 
-// Slot of a hi-byte bin in the shared window, or 255 when outside it.
-__device__ __forceinline__ uint32_t window_slot(uint32_t bin) {
-  const uint32_t m = bin ^ ((bin >> 7) * 0xF0u);  // 0xB0..0xBF -> 0x40..0x4F
-  return ((m >> 4) == 4u) ? ((m & 15u) | ((bin >> 7) << 4)) : 255u;
+// Shared-window slot of a hi byte (kDummy outside the window).
+__host__ __device__ constexpr uint32_t window_slot_of(uint32_t bin) {
+  return (((bin ^ ((bin >> 7) * 0xF0u)) >> 4) == 4u)
+             ? (((bin ^ ((bin >> 7) * 0xF0u)) & 15u) | ((bin >> 7) << 4))
+             : (uint32_t)kDummy;
 }
 
 __device__ __forceinline__ uint32_t slot_bin(int slot) {
   return slot < 16 ? 0x40u + slot : 0xB0u + (slot - 16);
 }
 
-
-// Shared-memory address of the x element f (flat index inside the tile) and
-// of the score element f.  fp32: in place.  bf16: x lives in the upper half
-// of the fp32 score area; writing score f only overwrites x elements below f.
-template <int E, typename T>
+// Shared-memory address of the x element f (flat index inside the tile).
+// fp32: in place.  bf16: x lives in the upper half of the fp32 score area;
+// writing score f only overwrites x elements below f.
+template <int E, typename T, int TILE>
 __device__ __forceinline__ T* x_ptr(unsigned char* tile, int f) {
   if constexpr (sizeof(T) == 4) {
     return reinterpret_cast<T*>(tile) + f;
   } else {
-    return reinterpret_cast<T*>(tile + kTile * E * 2) + f;
+    return reinterpret_cast<T*>(tile + TILE * E * 2) + f;
   }
 }
 
 // Rows of the next tile whose shared bytes are free once the scores of the
 // first F flat elements of this tile have been consumed.
-template <int E, typename T>
+template <int E, typename T, int TILE>
 __device__ __forceinline__ int rows_free(int F) {
   if constexpr (sizeof(T) == 4) {
     return F / E;
   } else {
-    const int r = (2 * F - kTile * E) / E;
-    return r < 0 ? 0 : (r > kTile ? kTile : r);
+    const int r = (2 * F - TILE * E) / E;
+    return r < 0 ? 0 : (r > TILE ? TILE : r);
   }
 }
 
-template <int E, typename T>
+template <int E, typename T, int TILE>
 __device__ __forceinline__ void issue_rows(unsigned char* tile, const T* logits, int64_t tile_start,
                                            int r0, int r1, uint64_t* bar) {
   if (r1 <= r0) return;
   fence_proxy_async_smem();
-  bulk_g2s(x_ptr<E, T>(tile, r0 * E), logits + (tile_start + r0) * (int64_t)E,
+  bulk_g2s(x_ptr<E, T, TILE>(tile, r0 * E), logits + (tile_start + r0) * (int64_t)E,
            (uint32_t)((r1 - r0) * E * sizeof(T)), bar);
 }
 
@@ -185,17 +193,46 @@ __device__ __forceinline__ void store8(float* p, const float (&x)[8]) {
   reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
 }
 
-template <int E, int KMAX, typename T, int MODE>
-__global__ void __launch_bounds__(Smem<E, T, MODE>::NW * 32, 1) route_kernel(const Args a) {
-  using GE = Geo<E>;
-  using SM = Smem<E, T, MODE>;
+// Eight margins alpha - s -> four packed key pairs.  `fold` maps margins that
+// round to bf16 -0 onto the +0 key; they only occur when some score is below
+// 2^-100 (a logit below -75), which phase A flags per tile.
+__device__ __forceinline__ void keys8(float alpha, const float (&s)[8], bool fold,
+                                      uint32_t (&kw)[4]) {
+  const f2_t A = f2_splat(alpha);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float r0, r1;
+    f2_unpack(f2_sub(A, f2_pack(s[2 * i], s[2 * i + 1])), r0, r1);
+    uint32_t w = bf16x2_rn(r0, r1);
+    if (fold) {
+      const uint32_t nz = (w & 0x7FFF7FFFu) + 0x7FFF7FFFu;
+      w &= (nz | 0x7FFF7FFFu);
+    }
+    kw[i] = w ^ (prmt(w, 0u, 0xBB99u) | 0x80008000u);
+  }
+}
+
+
+__device__ __forceinline__ void red_shared_add1(uint32_t addr) {
+  asm volatile("red.shared.add.u32 [%0], 1;" ::"r"(addr) : "memory");
+}
+
+__device__ __forceinline__ uint32_t lut_load(const uint8_t* lut, uint32_t bin) {
+  return lut[bin];
+}
+
+template <int E, int KMAX, bool EXACT, typename T, int MODE, int TILE>
+__global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kernel(const Args a) {
+  using GE = Geo<E, TILE>;
+  using SM = Smem<E, T, MODE, TILE>;
   constexpr int NW = SM::NW;
   extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ uint8_t lut[256];
+  __shared__ __align__(16) float bias_s[E];
   int32_t* hist_s = reinterpret_cast<int32_t*>(smem);
-  float* bias_s = reinterpret_cast<float*>(smem + SM::kHist);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  unsigned char* wbase = smem + SM::kFixed + warp * SM::kWarp;
+  unsigned char* wbase = smem + SM::kHist + warp * SM::kWarp;
   unsigned char* tile = wbase;
   float* sc = reinterpret_cast<float*>(tile);
   float* gmax = reinterpret_cast<float*>(wbase + SM::kTileBytes);
@@ -204,9 +241,10 @@ __global__ void __launch_bounds__(Smem<E, T, MODE>::NW * 32, 1) route_kernel(con
   const T* logits = static_cast<const T*>(a.logits);
   const int k = a.k;
 
-  // ---- prologue: zero the shared histogram, stage the bias, init barrier
+  // ---- prologue: zero the shared histogram, slot table, bias, barrier
   if constexpr (MODE == kModeHi) {
     for (int i = threadIdx.x; i < GE::NCOPY * GE::CSTRIDE; i += blockDim.x) hist_s[i] = 0;
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) lut[i] = (uint8_t)window_slot_of(i);
   }
   for (int i = threadIdx.x; i < E; i += blockDim.x) bias_s[i] = a.bias[i];
   if (lane == 0) {
@@ -216,14 +254,18 @@ __global__ void __launch_bounds__(Smem<E, T, MODE>::NW * 32, 1) route_kernel(con
   __syncthreads();
 
   // Per-lane expert block of the element-wise phases and its constants.
+  const int e0l = (E == 512) ? 8 * lane : (8 * lane) % E;
   float breg[GE::BREG];
   int32_t selreg[GE::BREG];
 #pragma unroll
   for (int i = 0; i < GE::BREG; ++i) {
-    const int e = (E == 512 ? (i >> 3) * 256 + 8 * lane : (8 * lane) % E) + (i & 7);
+    const int e = e0l + (i >> 3) * 256 + (i & 7);
     breg[i] = bias_s[e];
     selreg[i] = (MODE == kModeLo) ? a.sel[e] : 0;
   }
+  // shared byte address of this lane's counter for element i, slot 0
+  const int copy = (E >= 256) ? 0 : (8 * lane) / E;
+  const uint32_t hbase = smem_u32(hist_s) + 4u * (uint32_t)(copy * GE::CSTRIDE + (lane % GE::LPR));
   float k3_lo = 0.f, k3_scale = 0.f, k3_nb = 0.f;
   if constexpr (MODE == kModeK3) {
     k3_lo = a.bounds[0];
@@ -232,53 +274,59 @@ __global__ void __launch_bounds__(Smem<E, T, MODE>::NW * 32, 1) route_kernel(con
     k3_scale = __fdiv_rn(k3_nb, w);
   }
 
-  const int64_t n_tiles = (a.N + kTile - 1) / kTile;
+  const int64_t n_tiles = (a.N + TILE - 1) / TILE;
   const int64_t wstride = (int64_t)gridDim.x * NW;
   int64_t tix = (int64_t)blockIdx.x * NW + warp;
   uint32_t parity = 0;
   bool ok = true;
 
   if (tix < n_tiles && lane == 0) {
-    const int64_t t0 = tix * kTile;
-    const int rows = (int)((a.N - t0) < kTile ? (a.N - t0) : kTile);
+    const int64_t t0 = tix * TILE;
+    const int rows = (int)((a.N - t0) < TILE ? (a.N - t0) : TILE);
     mbar_arrive_expect_tx(bar, (uint32_t)(rows * E * sizeof(T)));
-    issue_rows<E, T>(tile, logits, t0, 0, rows, bar);
+    issue_rows<E, T, TILE>(tile, logits, t0, 0, rows, bar);
   }
 
   for (; tix < n_tiles && ok; tix += wstride) {
-    const int64_t t0 = tix * kTile;
-    const int rows = (int)((a.N - t0) < kTile ? (a.N - t0) : kTile);
+    const int64_t t0 = tix * TILE;
+    const int rows = (int)((a.N - t0) < TILE ? (a.N - t0) : TILE);
     const int64_t nt = tix + wstride;
-    const int64_t n0 = nt * kTile;
-    const int nrows = nt < n_tiles ? (int)((a.N - n0) < kTile ? (a.N - n0) : kTile) : 0;
+    const int64_t n0 = nt * TILE;
+    const int nrows = nt < n_tiles ? (int)((a.N - n0) < TILE ? (a.N - n0) : TILE) : 0;
 
     ok = mbar_wait_bounded(bar, parity, a.status);
     parity ^= 1u;
     if (!ok) break;
 
     // ---- phase A: scores in place, group maxima
+    bool ext = false;
 #pragma unroll 1
     for (int st = 0; st < GE::STEPS; ++st) {
       const int f = st * 256 + 8 * lane;
       const int row = f / E;
-      const int e0 = f % E;
+      const bool act = row < rows;
       float x[8];
-      if (row < rows) load8(x_ptr<E, T>(tile, f), x);
+      if (act) load8(x_ptr<E, T, TILE>(tile, f), x);
       if constexpr (sizeof(T) != 4) __syncwarp();
-      if (row < rows) {
+      if (act) {
         float s[8];
-        float g = -INFINITY;
+        const float m = sigmoid8(x, s);
+        ext |= m > kFoldAbsX;
+        const bool hi = (E == 512) && (st & 1);
+        float v[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          s[i] = sigmoid_pinned(x[i]);
-          const float b = (E == 512 && (st & 1)) ? breg[(8 + i) % GE::BREG] : breg[i];
-          g = fmaxf(g, __fadd_rn(s[i], b));
+        for (int i = 0; i < 4; ++i) {
+          const f2_t B = hi ? f2_pack(breg[(8 + 2 * i) % GE::BREG], breg[(9 + 2 * i) % GE::BREG])
+                            : f2_pack(breg[2 * i], breg[2 * i + 1]);
+          f2_unpack(f2_add(f2_pack(s[2 * i], s[2 * i + 1]), B), v[2 * i], v[2 * i + 1]);
         }
+        const float g = fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])),
+                              fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
         store8(sc + f, s);
-        gmax[row * GE::GP + (e0 >> 3)] = g;
+        gmax[row * GE::GP + ((f % E) >> 3)] = g;
       }
     }
-    __syncwarp();
+    const bool tile_ext = __any_sync(0xffffffffu, ext);
 
     // ---- phase B: one lane per token, alpha and the top-k set
     if (lane < rows) {
@@ -293,21 +341,27 @@ __global__ void __launch_bounds__(Smem<E, T, MODE>::NW * 32, 1) route_kernel(con
       for (int t = 0; t < KMAX; ++t) L[t] = -INFINITY;
 #pragma unroll
       for (int g = 0; g < GE::G; ++g) insert_desc<KMAX>(L, gm[g]);
-      const float tau = pick<KMAX>(L, k);
+      const float tau = pick<KMAX, EXACT>(L, k);
       uint64_t mask = 0;
 #pragma unroll
       for (int g = 0; g < GE::G; ++g) mask |= (gm[g] >= tau ? 1ull : 0ull) << g;
 #pragma unroll
       for (int t = 0; t < KMAX; ++t) L[t] = -INFINITY;
-      for (uint64_t m = mask; m; m &= m - 1) {
-        const int g = __ffsll((long long)m) - 1;
+      for (uint64_t mm = mask; mm; mm &= mm - 1) {
+        const int g = __ffsll((long long)mm) - 1;
         float s8[8], b8[8];
         load8(sc + lane * E + 8 * g, s8);
         load8(bias_s + 8 * g, b8);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) insert_desc<KMAX>(L, __fadd_rn(s8[i], b8[i]));
+        for (int i = 0; i < 4; ++i) {
+          float v0, v1;
+          f2_unpack(f2_add(f2_pack(s8[2 * i], s8[2 * i + 1]), f2_pack(b8[2 * i], b8[2 * i + 1])),
+                    v0, v1);
+          insert_desc<KMAX>(L, v0);
+          insert_desc<KMAX>(L, v1);
+        }
       }
-      const float alpha = pick<KMAX>(L, k);
+      const float alpha = pick<KMAX, EXACT>(L, k);
       alpha_s[lane] = alpha;
       const int64_t tok = t0 + lane;
       if (a.alpha_out) a.alpha_out[tok] = alpha;
@@ -318,8 +372,8 @@ __global__ void __launch_bounds__(Smem<E, T, MODE>::NW * 32, 1) route_kernel(con
         int ties = k - c_gt;
         int c = 0;
         int32_t* out = a.topk_out + tok * k;
-        for (uint64_t m = mask; m; m &= m - 1) {
-          const int g = __ffsll((long long)m) - 1;
+        for (uint64_t mm = mask; mm; mm &= mm - 1) {
+          const int g = __ffsll((long long)mm) - 1;
           float s8[8], b8[8];
           load8(sc + lane * E + 8 * g, s8);
           load8(bias_s + 8 * g, b8);
@@ -345,12 +399,13 @@ __global__ void __launch_bounds__(Smem<E, T, MODE>::NW * 32, 1) route_kernel(con
       const int f = st * 256 + 8 * lane;
       const int row = f / E;
       const int e0 = f % E;
-      if (row < rows) {
-        float s[8];
-        load8(sc + f, s);
-        const float alpha = alpha_s[row];
-        const int64_t tok = t0 + row;
-        if constexpr (MODE == kModeK3) {
+      const bool act = row < rows;
+      const int64_t tok = t0 + row;
+      if constexpr (MODE == kModeK3) {
+        if (act) {
+          float s[8];
+          load8(sc + f, s);
+          const float alpha = alpha_s[row];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float r = __fsub_rn(alpha, s[i]);
@@ -364,46 +419,61 @@ __global__ void __launch_bounds__(Smem<E, T, MODE>::NW * 32, 1) route_kernel(con
               idx = __float2int_rz(tt);
             atomicAdd(a.hist + (int64_t)(e0 + i) * a.nbins + idx, 1);
           }
-        } else {
-          uint32_t kw[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            kw[i] = keys_from_bf16x2(
-                bf16x2_rn(__fsub_rn(alpha, s[2 * i]), __fsub_rn(alpha, s[2 * i + 1])));
+        }
+      } else {
+        uint32_t kw[4] = {0u, 0u, 0u, 0u};
+        bool out_of_window = false;
+        if (act) {
+          float s[8];
+          load8(sc + f, s);
+          keys8(alpha_s[row], s, tile_ext, kw);
           if (MODE == kModeHi && a.keys_out)
             *reinterpret_cast<uint4*>(a.keys_out + tok * E + e0) =
                 make_uint4(kw[0], kw[1], kw[2], kw[3]);
+          if constexpr (MODE == kModeHi) {
+            const uint32_t hoff = (E == 512 && (st & 1)) ? 1024u : 0u;  // +256 experts
+            uint32_t mslot = 0;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint32_t key = (kw[i >> 1] >> ((i & 1) * 16)) & 0xFFFFu;
-            const uint32_t bin = key >> 8;
-            const int e = e0 + i;
-            if constexpr (MODE == kModeHi) {
-              const uint32_t slot = window_slot(bin);
-              if (slot < (uint32_t)kWin) {
-                const int copy = (E >= 256) ? 0 : (8 * lane) / E;
-                atomicAdd(hist_s + copy * GE::CSTRIDE + slot * E + GE::pi(e), 1);
-              } else {
-                atomicAdd(a.hist + (int64_t)e * 256 + bin, 1);
-              }
-            } else {
+            for (int i = 0; i < 8; ++i) {
+              const uint32_t bin = prmt(kw[i >> 1], 0u, (i & 1) ? 0x4443u : 0x4441u);
+              const uint32_t slot = lut_load(lut, bin);
+              mslot = slot > mslot ? slot : mslot;
+              red_shared_add1(hbase + hoff + 4u * (uint32_t)(i * GE::LPR) + slot * (4u * E));
+            }
+            out_of_window = mslot == (uint32_t)kDummy;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const uint32_t key = (kw[i >> 1] >> ((i & 1) * 16)) & 0xFFFFu;
               const int sl = (E == 512 && (st & 1)) ? selreg[(8 + i) % GE::BREG] : selreg[i];
-              if ((int)bin == sl) atomicAdd(a.hist + (int64_t)e * 256 + (key & 0xFFu), 1);
+              if ((int)(key >> 8) == sl)
+                atomicAdd(a.hist + (int64_t)(e0 + i) * 256 + (key & 0xFFu), 1);
+            }
+          }
+        }
+        if constexpr (MODE == kModeHi) {
+          // rare: hi bytes outside the shared window go to the global histogram
+          if (__any_sync(0xffffffffu, out_of_window) && out_of_window) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const uint32_t bin = prmt(kw[i >> 1], 0u, (i & 1) ? 0x4443u : 0x4441u);
+              if (lut_load(lut, bin) == (uint32_t)kDummy)
+                atomicAdd(a.hist + (int64_t)(e0 + i) * 256 + bin, 1);
             }
           }
         }
       }
       __syncwarp();
       if (lane == 0 && nrows > 0) {
-        int nf = rows_free<E, T>((st + 1) * 256);
+        int nf = rows_free<E, T, TILE>((st + 1) * 256);
         nf = nf < nrows ? nf : nrows;
-        issue_rows<E, T>(tile, logits, n0, copied, nf, bar);
+        issue_rows<E, T, TILE>(tile, logits, n0, copied, nf, bar);
         if (nf > copied) copied = nf;
       }
     }
   }
 
-  // ---- epilogue: flush the shared hi histogram
+  // ---- epilogue: flush the shared hi histogram (window slots only)
   if constexpr (MODE == kModeHi) {
     __syncthreads();
     for (int i = threadIdx.x; i < kWin * E; i += blockDim.x) {
@@ -419,11 +489,11 @@ __global__ void __launch_bounds__(Smem<E, T, MODE>::NW * 32, 1) route_kernel(con
   }
 }
 
-template <int E, int KMAX, typename T, int MODE>
+template <int E, int KMAX, bool EXACT, typename T, int MODE, int TILE>
 int launch_one(const Args& a, cudaStream_t stream) {
-  using SM = Smem<E, T, MODE>;
+  using SM = Smem<E, T, MODE, TILE>;
   static_assert(SM::NW >= 1, "tile does not fit shared memory");
-  auto kern = route_kernel<E, KMAX, T, MODE>;
+  auto kern = route_kernel<E, KMAX, EXACT, T, MODE, TILE>;
   static bool attr_set = false;  // per instantiation; benign race (idempotent)
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kTotal) !=
@@ -431,7 +501,7 @@ int launch_one(const Args& a, cudaStream_t stream) {
       return launch_status();
     attr_set = true;
   }
-  const int64_t n_tiles = (a.N + kTile - 1) / kTile;
+  const int64_t n_tiles = (a.N + TILE - 1) / TILE;
   int64_t grid = sm_count();
   const int64_t need = (n_tiles + SM::NW - 1) / SM::NW;
   if (need < grid) grid = need;
@@ -440,12 +510,14 @@ int launch_one(const Args& a, cudaStream_t stream) {
   return launch_status();
 }
 
-template <int MODE, typename T>
-int dispatch_E(int E, int kmax, const Args& a, cudaStream_t st) {
-#define QB_CASE(EE)                                                      \
-  case EE:                                                               \
-    return kmax <= 8 ? launch_one<EE, 8, T, MODE>(a, st)                 \
-                     : launch_one<EE, 16, T, MODE>(a, st);
+template <int MODE, typename T, int TILE>
+int dispatch_E(int E, int k, const Args& a, cudaStream_t st) {
+#define QB_CASE(EE)                                                       \
+  case EE:                                                                \
+    if (k + 1 == 7) return launch_one<EE, 7, true, T, MODE, TILE>(a, st); \
+    if (k + 1 == 9) return launch_one<EE, 9, true, T, MODE, TILE>(a, st); \
+    if (k + 1 <= 8) return launch_one<EE, 8, false, T, MODE, TILE>(a, st); \
+    return launch_one<EE, 16, false, T, MODE, TILE>(a, st);
   switch (E) {
     QB_CASE(32)
     QB_CASE(64)
@@ -458,6 +530,10 @@ int dispatch_E(int E, int kmax, const Args& a, cudaStream_t st) {
 #undef QB_CASE
 }
 
+#ifndef QB_ROUTE_TILE
+#define QB_ROUTE_TILE 32
+#endif
+
 template <int MODE>
 int launch_mode(const void* logits, int dtype, const float* bias, int64_t N, int E, int k,
                 int32_t* hist, uint16_t* keys_out, int32_t* topk_out, float* alpha_out,
@@ -465,8 +541,8 @@ int launch_mode(const void* logits, int dtype, const float* bias, int64_t N, int
   Args a{logits, bias, N, k, hist, keys_out, topk_out, alpha_out, sel, bounds, nbins,
          device_status_ptr()};
   if (!a.status) return QB_ECUDA;
-  if (dtype == QB_F32) return dispatch_E<MODE, float>(E, k + 1, a, stream);
-  return dispatch_E<MODE, __nv_bfloat16>(E, k + 1, a, stream);
+  if (dtype == QB_F32) return dispatch_E<MODE, float, QB_ROUTE_TILE>(E, k, a, stream);
+  return dispatch_E<MODE, __nv_bfloat16, QB_ROUTE_TILE>(E, k, a, stream);
 }
 
 }  // namespace route

@@ -72,7 +72,11 @@ int64_t qb_rank(int64_t n_pool, int E, int k);
 
 /* Pinned logistic function, element-wise: s[i] = sigma(x[i]) as the fixed
  * binary32 operation sequence the routing kernels use ([QB-PR] "raw sigmoid
- * router score").  x, s: device fp32 [n]; may alias. */
+ * router score"):  s = RN(1 / RN(1 + RN(p(w) * 2^n))) with n = rint(-x*log2 e),
+ * w = x + n*ln2 (Cody-Waite, two fma), p = degree-7 Taylor polynomial of
+ * exp(-w) in Horner/fma form; x clamped to [-104, 104].  Computed by the same
+ * device code as the routing kernels (chunks of 8).  x, s: device fp32 [n];
+ * may alias. */
 int qb_sigmoid(const float* x, float* s, int64_t n, void* stream);
 
 /* Fill n int32 values with zero (a convenience for histograms). */

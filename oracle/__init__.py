@@ -67,7 +67,7 @@ def _load():
         sigs = {
             "orc_sigmoid": (F, [F]),
             "orc_sigmoid_array": (None, [P, P, I64]),
-            "orc_exp_neg_abs": (F, [F]),
+            "orc_exp_neg": (F, [F]),
             "orc_exp_coeffs": (None, [P]),
             "orc_bf16_rne": (ctypes.c_uint16, [F]),
             "orc_key": (ctypes.c_uint16, [F]),
@@ -115,8 +115,8 @@ def sigmoid(x) -> np.ndarray:
     return out
 
 
-def exp_neg_abs(x: float) -> float:
-    return float(_load().orc_exp_neg_abs(float(x)))
+def exp_neg(x: float) -> float:
+    return float(_load().orc_exp_neg(float(x)))
 
 
 def exp_coeffs() -> np.ndarray:

@@ -24,22 +24,19 @@
 /* estimator").  Histogram counts are integers decided by fp32 margins, so    */
 /* the score must be one fixed, reproducible binary32 function.  This is it: */
 /*                                                                           */
-/*   a  = min(|x|, 104)             (exp(-104) is below half the least       */
-/*                                   subnormal, so larger |x| changes nothing)*/
-/*   z  = -a                                                                  */
-/*   t  = fma(z, L2E, M)            M = 1.5*2^23: t - M = rint(z*log2 e) = n  */
+/*   x  = clamp(x, -104, 104)       (beyond, exp(-x) over/underflows anyway) */
+/*   t  = fma(x, -L2E, M)           M = 1.5*2^23: n = t - M = rint(-x*log2 e)*/
 /*   n  = t - M                     (exact)                                   */
-/*   u  = fma(n, -LN2_HI, z)        Cody & Waite (1980) two-part reduction    */
-/*   u  = fma(n, -LN2_LO, u)                                                  */
-/*   p  = sum_{i=0..7} u^i / i!     degree-7 Taylor polynomial of exp(u),     */
-/*                                  Horner form, one fma per degree,          */
-/*                                  coefficients RN(1/i!)                     */
-/*   e  = RN(p * 2^n)               (a single rounding; exact unless the      */
-/*                                   result is subnormal)                     */
-/*   d  = RN(1 + e)                                                           */
-/*   s  = RN(num / d),  num = 1 if x >= 0 else e   (correctly rounded divide) */
+/*   w  = fma(n, LN2_HI, x)         Cody & Waite (1980) two-part reduction:   */
+/*   w  = fma(n, LN2_LO, w)         w = x + n*ln2, so exp(-x) = 2^n*exp(-w)   */
+/*   p  = sum_{i=0..7} (-w)^i / i!  degree-7 Taylor polynomial of exp(-w),    */
+/*                                  Horner form in w, one fma per degree,     */
+/*                                  coefficients RN((-1)^i / i!)              */
+/*   e  = RN(p * 2^n)               (one rounding; +inf when it overflows)    */
+/*   s  = RN(1 / RN(1 + e))         (correctly rounded reciprocal)            */
 /*                                                                           */
-/* so s = 1/(1+exp(-x)) for x >= 0 and exp(x)/(1+exp(x)) for x < 0.          */
+/* so s = 1/(1+exp(-x)); for x < -88.72 e overflows and s = 0 (the exact     */
+/* value there is below 3e-39).                                              */
 /* ------------------------------------------------------------------------ */
 
 static const float kL2E = 0x1.715476p+0f;     /* RN(log2(e)) */
@@ -48,40 +45,39 @@ static const float kLn2Hi = 0x1.62e4p-1f;     /* 0.693145751953125 */
 static const float kLn2Lo = 0x1.7f7d1cp-20f;  /* RN(ln 2 - kLn2Hi) */
 
 static const float kExpCoef[8] = {
-    0x1.0p+0f,       /* 1/0! */
-    0x1.0p+0f,       /* 1/1! */
-    0x1.0p-1f,       /* 1/2! */
-    0x1.555556p-3f,  /* 1/3! */
-    0x1.555556p-5f,  /* 1/4! */
-    0x1.111112p-7f,  /* 1/5! */
-    0x1.6c16c2p-10f, /* 1/6! */
-    0x1.a01a02p-13f, /* 1/7! */
+    0x1.0p+0f,        /* +1/0! */
+    -0x1.0p+0f,       /* -1/1! */
+    0x1.0p-1f,        /* +1/2! */
+    -0x1.555556p-3f,  /* -1/3! */
+    0x1.555556p-5f,   /* +1/4! */
+    -0x1.111112p-7f,  /* -1/5! */
+    0x1.6c16c2p-10f,  /* +1/6! */
+    -0x1.a01a02p-13f, /* -1/7! */
 };
 
 void orc_exp_coeffs(float* c8) {
   for (int i = 0; i < 8; ++i) c8[i] = kExpCoef[i];
 }
 
-float orc_exp_neg_abs(float x) {
-  float a = fabsf(x);
-  if (a > 104.0f) a = 104.0f;
-  float z = -a;
-  float t = fmaf(z, kL2E, kMagic);
+float orc_exp_neg(float x) {
+  float xc = x;
+  if (xc > 104.0f) xc = 104.0f;
+  if (xc < -104.0f) xc = -104.0f;
+  float t = fmaf(xc, -kL2E, kMagic);
   float n = t - kMagic;
-  float u = fmaf(n, -kLn2Hi, z);
-  u = fmaf(n, -kLn2Lo, u);
+  float w = fmaf(n, kLn2Hi, xc);
+  w = fmaf(n, kLn2Lo, w);
   float p = kExpCoef[7];
-  for (int i = 6; i >= 0; --i) p = fmaf(p, u, kExpCoef[i]);
-  /* RN(p * 2^n): the product is exact in binary64 (n >= -151), and the cast
-   * to binary32 rounds it once. */
+  for (int i = 6; i >= 0; --i) p = fmaf(p, w, kExpCoef[i]);
+  /* RN(p * 2^n): the product is exact in binary64 (|n| <= 151), and the cast
+   * to binary32 rounds it once (to +inf on overflow). */
   return (float)ldexp((double)p, (int)n);
 }
 
 float orc_sigmoid(float x) {
-  float e = orc_exp_neg_abs(x);
+  float e = orc_exp_neg(x);
   float d = 1.0f + e;
-  float num = (x >= 0.0f) ? 1.0f : e;
-  return num / d;
+  return 1.0f / d;
 }
 
 void orc_sigmoid_array(const float* x, float* s, int64_t n) {

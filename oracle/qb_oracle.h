@@ -31,9 +31,9 @@ extern "C" {
  * "Quantile estimator").  See qb_oracle.c for the exact operation sequence. */
 float orc_sigmoid(float x);
 void orc_sigmoid_array(const float* x, float* s, int64_t n);
-/* The exp(-|x|) stage of orc_sigmoid, exposed for accuracy tests. */
-float orc_exp_neg_abs(float x);
-/* Taylor coefficients used by the exp stage, c[0..7] = RN(1/i!). */
+/* The exp(-x) stage of orc_sigmoid, exposed for accuracy tests. */
+float orc_exp_neg(float x);
+/* Taylor coefficients used by the exp stage, c[0..7] = RN((-1)^i / i!). */
 void orc_exp_coeffs(float* c8);
 
 /* fp32 -> bf16 bit pattern, round to nearest, ties to even. */

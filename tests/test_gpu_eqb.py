@@ -75,9 +75,11 @@ def test_route_extreme_logits(qb, orc):
     # to bf16 -0 (folded to the +0 key), saturated scores of exactly 1.
     E, k, N = 64, 6, 96
     x, b = _logits(N, E, seed=5)
-    x[0:32] = -100.0 + torch.rand(32, E, device="cuda") * 5.0
+    # scores a few subnormal ulps apart: margins round to bf16 -0
+    x[0:32] = -88.0 + (torch.rand(32, E, device="cuda") - 0.5) * 1e-5
     x[32:48] = 90.0 + torch.rand(16, E, device="cuda") * 20.0
     x[48:64, ::3] = -120.0
+    x[64:80] = -100.0 + torch.rand(16, E, device="cuda") * 20.0
     b[:] = 0.0
     res = gpu_route(qb, x.contiguous(), b, k)
     ref = assert_route_matches(orc, res, host_logits(x), b.cpu().numpy(), k)

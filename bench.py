@@ -128,7 +128,7 @@ class FullStep:
         self.topk = torch.empty(n, k, dtype=torch.int32, device=dev)
         self.ws = torch.empty(w.n_micro, E, dtype=torch.float32, device=dev)
         self.R = qb.rank(n, E, k)
-        self.launches_per_layer = {"eqb": 6, "lei": 2}
+        self.launches_per_layer = {"eqb": 5, "lei": 2}
         self.hi_events = []
 
     def layer(self, l, logits=None, grad=None, lei=True, time_hi=False):

@@ -70,11 +70,11 @@ __device__ __forceinline__ float sigmoid_pinned(float x) {
   const int ni = __float2int_rz(n);  // exact: n is an integer in [-151, 151]
   float e;
   if (ni >= -125 && ni <= 126) {
-    e = __int_as_float(__float_as_int(p) + (ni << 23));
+    e = __uint_as_float(__float_as_uint(p) + ((unsigned)ni << 23));
   } else if (ni > 126) {  // exact scale into range, then one rounding (may overflow)
-    e = __fmul_rn(__int_as_float(__float_as_int(p) + ((ni - 64) << 23)), 0x1.0p+64f);
+    e = __fmul_rn(__uint_as_float(__float_as_uint(p) + ((unsigned)(ni - 64) << 23)), 0x1.0p+64f);
   } else {  // may be subnormal: one rounding
-    e = __fmul_rn(__int_as_float(__float_as_int(p) + ((ni + 64) << 23)), 0x1.0p-64f);
+    e = __fmul_rn(__uint_as_float(__float_as_uint(p) + ((unsigned)(ni + 64) << 23)), 0x1.0p-64f);
   }
   return __frcp_rn(__fadd_rn(1.0f, e));
 }
@@ -115,9 +115,10 @@ __device__ __forceinline__ float rcp_approx(float d) {
 }
 
 // Pinned sigmoid of two inputs with |x| <= kFastAbsX.  The reciprocal is
-// RN(1/d) from a hardware estimate refined by two Newton steps
-// y <- y + y*(1 - d*y) in fma form (Markstein's method); equality with the
-// correctly rounded reciprocal is verified on every binary32 input.
+// RN(1/d) from the hardware estimate refined by one Newton step
+// y <- y + y*(1 - d*y) in fma form (Markstein's method).  That this equals
+// the correctly rounded reciprocal for every d this function can produce is
+// checked by running it on every binary32 input against the oracle.
 __device__ __forceinline__ f2_t sigmoid2_fast(f2_t X) {
   const f2_t T = f2_fma(X, f2_splat(-kL2E), f2_splat(kMagic));
   const f2_t N = f2_sub(T, f2_splat(kMagic));
@@ -135,18 +136,15 @@ __device__ __forceinline__ f2_t sigmoid2_fast(f2_t X) {
   f2_unpack(T, t0, t1);
   // t = 1.5*2^23 + n, and (bits(1.5*2^23) << 23) == 0 mod 2^32, so
   // (bits(t) << 23) == n << 23: adding it to p's exponent multiplies by 2^n.
-  const float e0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
-  const float e1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
+  const float e0 = __uint_as_float(__float_as_uint(t0) * 0x800000u + __float_as_uint(p0));
+  const float e1 = __uint_as_float(__float_as_uint(t1) * 0x800000u + __float_as_uint(p1));
   const f2_t D = f2_add(f2_pack(e0, e1), f2_splat(1.0f));
   const f2_t ND = f2_sub(f2_splat(0.0f), D);
   float d0, d1;
   f2_unpack(D, d0, d1);
-  f2_t Y = f2_pack(rcp_approx(d0), rcp_approx(d1));
-  f2_t R = f2_fma(ND, Y, f2_splat(1.0f));
-  Y = f2_fma(R, Y, Y);
-  R = f2_fma(ND, Y, f2_splat(1.0f));
-  Y = f2_fma(R, Y, Y);
-  return Y;
+  const f2_t Y = f2_pack(rcp_approx(d0), rcp_approx(d1));
+  const f2_t R = f2_fma(ND, Y, f2_splat(1.0f));
+  return f2_fma(R, Y, Y);
 }
 
 // Eight inputs in registers -> eight scores; the fast path when all |x| are

@@ -65,11 +65,20 @@ __global__ void __launch_bounds__(kLoThreads, 1)
     // flat element range of this epoch, in 256-element warp steps
     const int64_t f_begin = ep * E, f_end = ep_end * E;
     const int64_t steps = (f_end - f_begin + 255) / 256;
-    for (int64_t st = warp; st < steps; st += kWarps) {
-      const int64_t f = f_begin + st * 256 + 8 * lane;
-      if (f < f_end) {
-        const uint4 u = __ldcs(reinterpret_cast<const uint4*>(keys + f));
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    constexpr int kU = 4;  // 16-byte chunks in flight per lane
+    for (int64_t st0 = (int64_t)warp * kU; st0 < steps; st0 += (int64_t)kWarps * kU) {
+      uint4 u[kU];
+#pragma unroll
+      for (int q = 0; q < kU; ++q) {
+        const int64_t f = f_begin + (st0 + q) * 256 + 8 * lane;
+        u[q] = (f < f_end) ? __ldcs(reinterpret_cast<const uint4*>(keys + f))
+                           : make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
+      }
+#pragma unroll
+      for (int q = 0; q < kU; ++q) {
+        const int64_t f = f_begin + (st0 + q) * 256 + 8 * lane;
+        if (f >= f_end) continue;
+        const uint32_t w[4] = {u[q].x, u[q].y, u[q].z, u[q].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const uint32_t x = w[i] ^ pat[i];
@@ -149,17 +158,68 @@ __global__ void __launch_bounds__(256) select_hi_kernel(const int32_t* __restric
 }
 
 // ------------------------------------------------------------------------
-// EQB finalize: one CTA of 1024 threads.  Warp w handles experts w, w+32, ...:
-// lo select by a warp scan over the 256 lo bins, key -> bf16 value; then
-// thread 0 sums the values in fp64 in ascending expert order.
+// EQB finalize, two kernels.
+// eqb_lo_select_kernel: one CTA (256 threads) per expert.  Block scan of the
+//   lo histogram row, first bin reaching r_lo, key -> bf16 value q_j written
+//   to bias_out[j] (a staging slot), key to qkey_out; with reset the CTA then
+//   zeroes its own hist_hi and hist_lo rows in place.
+// eqb_center_kernel: one CTA.  mu = (sum_j q_j in fp64, ascending j) / E,
+//   bias_out[j] = RN32(q_j - mu).
 // ------------------------------------------------------------------------
 __device__ __forceinline__ float key_decode(uint32_t key) {
   const uint32_t h = (key & 0x8000u) ? (key ^ 0x8000u) : (key ^ 0xFFFFu);
   return __uint_as_float((h & 0xFFFFu) << 16);
 }
 
-// First index (0..255) where the inclusive prefix sum of the row reaches
-// `target`, or -1; `before` receives the sum of the bins below it.  One warp.
+__global__ void __launch_bounds__(256) eqb_lo_select_kernel(
+    int32_t* __restrict__ hist_hi, int32_t* __restrict__ hist_lo, const int32_t* __restrict__ sel,
+    const int32_t* __restrict__ r_lo, float* __restrict__ bias_out,
+    uint16_t* __restrict__ qkey_out, int reset) {
+  __shared__ long long tmp[8];
+  __shared__ int lo_s;
+  const int j = blockIdx.x;
+  const int b = threadIdx.x;
+  const int sj = sel[j];
+  const long long target = r_lo[j];
+  const long long c = hist_lo[(int64_t)j * 256 + b];
+  if (b == 0) lo_s = -1;
+  const long long cum = block_inclusive_scan256(c, tmp);  // contains __syncthreads
+  if (cum >= target && cum - c < target) lo_s = b;
+  __syncthreads();
+  if (b == 0) {
+    const int lo = lo_s;
+    if (sj >= 0 && lo >= 0) {
+      const uint32_t key = ((uint32_t)sj << 8) | (uint32_t)lo;
+      bias_out[j] = key_decode(key);
+      if (qkey_out) qkey_out[j] = (uint16_t)key;
+    } else {
+      bias_out[j] = __int_as_float(0x7FC00000);  // rank beyond the pooled count
+      if (qkey_out) qkey_out[j] = 0;
+    }
+  }
+  if (reset) {
+    hist_lo[(int64_t)j * 256 + b] = 0;
+    hist_hi[(int64_t)j * 256 + b] = 0;
+  }
+}
+
+__global__ void __launch_bounds__(512) eqb_center_kernel(float* __restrict__ bias_out, int E) {
+  __shared__ float q_s[512];
+  __shared__ double mu_s;
+  for (int j = threadIdx.x; j < E; j += blockDim.x) q_s[j] = bias_out[j];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double sum = 0.0;
+    for (int j = 0; j < E; ++j) sum = __dadd_rn(sum, (double)q_s[j]);
+    mu_s = __ddiv_rn(sum, (double)E);
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < E; j += blockDim.x)
+    bias_out[j] = __double2float_rn(__dsub_rn((double)q_s[j], mu_s));
+}
+
+// First index where the inclusive prefix sum of the row reaches `target`, or
+// -1; `before` receives the sum of the bins below it.  One warp.
 __device__ int warp_first_reaching(const int32_t* __restrict__ row, int nbins, long long target,
                                    long long* before_out) {
   const int lane = threadIdx.x & 31;
@@ -186,40 +246,6 @@ __device__ int warp_first_reaching(const int32_t* __restrict__ row, int nbins, l
   }
   *before_out = base;
   return -1;
-}
-
-__global__ void __launch_bounds__(1024) eqb_finalize_kernel(
-    const int32_t* __restrict__ hist_lo, const int32_t* __restrict__ sel,
-    const int32_t* __restrict__ r_lo, int E, float* __restrict__ bias_out,
-    uint16_t* __restrict__ qkey_out) {
-  __shared__ float q_s[512];
-  __shared__ double mu_s;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int j = warp; j < E; j += 32) {
-    const int sj = sel[j];
-    long long before = 0;
-    const int lo = (sj >= 0) ? warp_first_reaching(hist_lo + (int64_t)j * 256, 256, r_lo[j], &before)
-                             : -1;
-    if (lane == 0) {
-      if (sj >= 0 && lo >= 0) {
-        const uint32_t key = ((uint32_t)sj << 8) | (uint32_t)lo;
-        q_s[j] = key_decode(key);
-        if (qkey_out) qkey_out[j] = (uint16_t)key;
-      } else {
-        q_s[j] = __int_as_float(0x7FC00000);  // rank beyond the pooled count
-        if (qkey_out) qkey_out[j] = 0;
-      }
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double sum = 0.0;
-    for (int j = 0; j < E; ++j) sum = __dadd_rn(sum, (double)q_s[j]);
-    mu_s = __ddiv_rn(sum, (double)E);
-  }
-  __syncthreads();
-  for (int j = threadIdx.x; j < E; j += blockDim.x)
-    bias_out[j] = __double2float_rn(__dsub_rn((double)q_s[j], mu_s));
 }
 
 // ------------------------------------------------------------------------
@@ -369,12 +395,12 @@ int launch_zero_i32(int32_t* p, int64_t n, cudaStream_t stream) {
 
 int launch_finalize(int32_t* hist_hi, int32_t* hist_lo, const int32_t* sel, const int32_t* r_lo,
                     int E, float* bias_out, uint16_t* qkey_out, int reset, cudaStream_t stream) {
-  eqb_finalize_kernel<<<1, 1024, 0, stream>>>(hist_lo, sel, r_lo, E, bias_out, qkey_out);
+  eqb_lo_select_kernel<<<E, 256, 0, stream>>>(hist_hi, hist_lo, sel, r_lo, bias_out, qkey_out,
+                                              reset);
   int st = launch_status();
-  if (st != QB_OK || !reset) return st;
-  st = launch_zero_i32(hist_hi, (int64_t)E * 256, stream);
   if (st != QB_OK) return st;
-  return launch_zero_i32(hist_lo, (int64_t)E * 256, stream);
+  eqb_center_kernel<<<1, 512, 0, stream>>>(bias_out, E);
+  return launch_status();
 }
 
 int launch_k3_finalize(int32_t* hist, int E, int nbins, int64_t r, float* bounds,

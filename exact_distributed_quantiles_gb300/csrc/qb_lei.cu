@@ -21,30 +21,64 @@ namespace qb {
 namespace {
 
 constexpr int kRhoThreads = 1024;
+constexpr int kRhoWarps = kRhoThreads / 32;
 
+// One CTA per local batch.  Top-k entries are read 16 at a time per thread
+// (four 16-byte loads in flight) and counted in per-warp shared histograms,
+// which are summed at the end.
 __global__ void __launch_bounds__(kRhoThreads) lei_rho_kernel(const int32_t* __restrict__ topk,
                                                               int64_t N, int E, int k, float eta,
                                                               int64_t batch_tokens,
                                                               float* __restrict__ ws) {
-  __shared__ int32_t load_s[512];
+  extern __shared__ int32_t sub[];  // [kRhoWarps][E]
   __shared__ double t_s[512];
   __shared__ double mean_s;
+  const int warp = threadIdx.x >> 5;
   const int64_t b = blockIdx.x;
   const int64_t i0 = b * batch_tokens;
   int64_t i1 = i0 + batch_tokens;
   if (i1 > N) i1 = N;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) load_s[e] = 0;
+  for (int q = threadIdx.x; q < kRhoWarps * E; q += blockDim.x) sub[q] = 0;
   __syncthreads();
+  int32_t* mine = sub + warp * E;
   const int64_t n_idx = (i1 - i0) * k;
   const int32_t* t = topk + i0 * k;
-  for (int64_t q = threadIdx.x; q < n_idx; q += blockDim.x) {
-    const int32_t e = __ldcs(t + q);
-    if ((unsigned)e < (unsigned)E) atomicAdd(&load_s[e], 1);
+  // scalar head until 16-byte alignment, then int4 body, then scalar tail
+  const int64_t head = ((16 - (reinterpret_cast<uintptr_t>(t) & 15)) & 15) / 4;
+  const int64_t h = head < n_idx ? head : n_idx;
+  for (int64_t q = threadIdx.x; q < h; q += blockDim.x) {
+    const int32_t e = t[q];
+    if ((unsigned)e < (unsigned)E) atomicAdd(&mine[e], 1);
+  }
+  const int4* t4 = reinterpret_cast<const int4*>(t + h);
+  const int64_t n4 = (n_idx - h) / 4;
+  constexpr int kU = 4;
+  for (int64_t q0 = threadIdx.x; q0 < n4; q0 += (int64_t)blockDim.x * kU) {
+    int4 v[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t q = q0 + (int64_t)u * blockDim.x;
+      v[u] = q < n4 ? __ldcs(t4 + q) : make_int4(-1, -1, -1, -1);
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int32_t ev[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if ((unsigned)ev[c] < (unsigned)E) atomicAdd(&mine[ev[c]], 1);
+    }
+  }
+  for (int64_t q = h + 4 * n4 + threadIdx.x; q < n_idx; q += blockDim.x) {
+    const int32_t e = t[q];
+    if ((unsigned)e < (unsigned)E) atomicAdd(&mine[e], 1);
   }
   __syncthreads();
   const double T = __ddiv_rn((double)((i1 - i0) * (int64_t)k), (double)E);
-  for (int e = threadIdx.x; e < E; e += blockDim.x)
-    t_s[e] = tanh(__ddiv_rn(__dsub_rn((double)load_s[e], T), T));
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int32_t load = 0;
+    for (int w = 0; w < kRhoWarps; ++w) load += sub[w * E + e];
+    t_s[e] = tanh(__ddiv_rn(__dsub_rn((double)load, T), T));
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     double sum = 0.0;
@@ -56,24 +90,48 @@ __global__ void __launch_bounds__(kRhoThreads) lei_rho_kernel(const int32_t* __r
     ws[b * E + e] = __double2float_rn(__dmul_rn((double)eta, __dsub_rn(t_s[e], mean_s)));
 }
 
-__global__ void __launch_bounds__(256) lei_apply_kernel(float* __restrict__ grad, int64_t N,
-                                                        int E, int64_t batch_tokens,
-                                                        const float* __restrict__ ws) {
-  const int64_t n4 = N * (int64_t)E / 4;
-  const int e4 = E / 4;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+// grad += c[batch(row)] streamed in 16-byte chunks.  Each CTA walks whole
+// rows (32-bit row arithmetic, one division per row), four chunks in flight
+// per thread.
+constexpr int kApplyThreads = 256;
+
+__global__ void __launch_bounds__(kApplyThreads) lei_apply_kernel(float* __restrict__ grad,
+                                                                  int N, int e4_log2,
+                                                                  int batch_tokens,
+                                                                  const float* __restrict__ ws) {
+  const int e4 = 1 << e4_log2;                 // 16-byte chunks per row
+  const int rows_per_pass = kApplyThreads >> e4_log2 ? kApplyThreads >> e4_log2 : 1;
+  const int lanes_per_row = kApplyThreads < e4 ? kApplyThreads : e4;
+  const int r_in = threadIdx.x >> (e4_log2 < 8 ? e4_log2 : 8);
+  const int c_in = threadIdx.x & (lanes_per_row - 1);
   float4* g4 = reinterpret_cast<float4*>(grad);
   const float4* c4 = reinterpret_cast<const float4*>(ws);
-  for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n4; q += stride) {
-    const int64_t row = q / e4;
-    const int col = (int)(q - row * e4);
-    const float4 c = __ldg(c4 + (row / batch_tokens) * e4 + col);
-    float4 g = __ldcs(g4 + q);
-    g.x = __fadd_rn(g.x, c.x);
-    g.y = __fadd_rn(g.y, c.y);
-    g.z = __fadd_rn(g.z, c.z);
-    g.w = __fadd_rn(g.w, c.w);
-    __stcs(g4 + q, g);
+  constexpr int kU = 4;
+  const int64_t stride = (int64_t)gridDim.x * rows_per_pass * kU;
+  for (int64_t r0 = (int64_t)blockIdx.x * rows_per_pass * kU; r0 < N; r0 += stride) {
+    for (int col = c_in; col < e4; col += lanes_per_row) {
+      float4 g[kU], c[kU];
+      int rr[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        rr[u] = (int)(r0 + u * rows_per_pass + r_in);
+        if (rr[u] < N) {
+          g[u] = __ldcs(g4 + ((int64_t)rr[u] << e4_log2) + col);
+          c[u] = __ldg(c4 + ((int64_t)(rr[u] / batch_tokens) << e4_log2) + col);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        if (rr[u] < N) {
+          float4 o;
+          o.x = __fadd_rn(g[u].x, c[u].x);
+          o.y = __fadd_rn(g[u].y, c[u].y);
+          o.z = __fadd_rn(g[u].z, c[u].z);
+          o.w = __fadd_rn(g[u].w, c[u].w);
+          __stcs(g4 + ((int64_t)rr[u] << e4_log2) + col, o);
+        }
+      }
+    }
   }
 }
 
@@ -82,16 +140,27 @@ __global__ void __launch_bounds__(256) lei_apply_kernel(float* __restrict__ grad
 int launch_lei(float* grad, const int32_t* topk, int64_t N, int E, int k, float eta,
                int64_t batch_tokens, float* workspace, cudaStream_t stream) {
   const int64_t nb = (N + batch_tokens - 1) / batch_tokens;
-  lei_rho_kernel<<<(unsigned)nb, kRhoThreads, 0, stream>>>(topk, N, E, k, eta, batch_tokens,
-                                                          workspace);
+  const int smem = kRhoWarps * E * (int)sizeof(int32_t);
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(lei_rho_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kRhoWarps * 512 * (int)sizeof(int32_t)) != cudaSuccess)
+      return launch_status();
+    attr = true;
+  }
+  lei_rho_kernel<<<(unsigned)nb, kRhoThreads, smem, stream>>>(topk, N, E, k, eta, batch_tokens,
+                                                             workspace);
   int st = launch_status();
   if (st != QB_OK) return st;
-  const int64_t n4 = N * (int64_t)E / 4;
-  int64_t grid = (n4 + 255) / 256;
+  int e4_log2 = 0;
+  while ((1 << e4_log2) < E / 4) ++e4_log2;  // E is a power of two
+  const int rows_per_pass = (kApplyThreads >> e4_log2) ? (kApplyThreads >> e4_log2) : 1;
+  int64_t grid = (N + rows_per_pass * 4 - 1) / (rows_per_pass * 4);
   const int64_t gmax = (int64_t)sm_count() * 8;
   if (grid > gmax) grid = gmax;
   if (grid < 1) grid = 1;
-  lei_apply_kernel<<<(unsigned)grid, 256, 0, stream>>>(grad, N, E, batch_tokens, workspace);
+  lei_apply_kernel<<<(unsigned)grid, kApplyThreads, 0, stream>>>(grad, (int)N, e4_log2,
+                                                                (int)batch_tokens, workspace);
   return launch_status();
 }
 

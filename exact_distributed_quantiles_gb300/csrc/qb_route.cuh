@@ -43,6 +43,10 @@ namespace route {
 constexpr int kWin = 32;      // hi-byte bins privatised in shared memory
 constexpr int kDummy = kWin;  // slot of every other bin (never flushed)
 constexpr int kSmemLimit = 227 * 1024;
+#ifndef QB_UNROLL_A
+#define QB_UNROLL_A 1
+#endif
+constexpr int kUnrollA = QB_UNROLL_A;  // phase-A steps unrolled (ILP)
 
 struct Args {
   const void* logits;
@@ -92,7 +96,7 @@ struct Smem {
   static constexpr int kStatic = 256 + E * 4 + 1024;  // static lut + bias, and a margin
   static constexpr int kFixed = kHist + kStatic;
   static constexpr int kTileBytes = TILE * E * 4;  // fp32 scores; bf16 input sits in the upper half
-  static constexpr int kGmax = round16(TILE * GE::GP * 4);
+  static constexpr int kGmax = round16(TILE * (GE::GP > 16 ? GE::GP : 16) * 4);
   static constexpr int kAlpha = round16(TILE * 4);
   static constexpr int kWarp = kTileBytes + kGmax + kAlpha + 16;  // + mbarrier
   static constexpr int nw_fit() {
@@ -103,26 +107,73 @@ struct Smem {
   static constexpr int kTotal = kHist + NW * kWarp;  // dynamic shared memory
 };
 
-// Insert v into the descending list L[0..KMAX) (drops the smallest).
-template <int KMAX>
-__device__ __forceinline__ void insert_desc(float (&L)[KMAX], float v) {
+// ---- register selection networks (all descending) ----
+__device__ __forceinline__ void cas_desc(float& a, float& b) {
+  const float hi = fmaxf(a, b);
+  b = fminf(a, b);
+  a = hi;
+}
+
+// Insert v into the descending list L[0..KL) (drops the smallest).
+template <int KL>
+__device__ __forceinline__ void insert_desc(float (&L)[KL], float v) {
 #pragma unroll
-  for (int t = 0; t < KMAX; ++t) {
-    const float hi = fmaxf(L[t], v);
-    v = fminf(L[t], v);
-    L[t] = hi;
+  for (int t = 0; t < KL; ++t) cas_desc(L[t], v);
+}
+
+// Sort 8 values descending: a 19-comparator network (checked on all 0/1
+// inputs, which by the 0-1 principle covers every input).
+__device__ __forceinline__ void sort8_desc(float (&v)[8]) {
+  cas_desc(v[0], v[2]); cas_desc(v[1], v[3]); cas_desc(v[4], v[6]); cas_desc(v[5], v[7]);
+  cas_desc(v[0], v[4]); cas_desc(v[1], v[5]); cas_desc(v[2], v[6]); cas_desc(v[3], v[7]);
+  cas_desc(v[0], v[1]); cas_desc(v[2], v[3]); cas_desc(v[4], v[5]); cas_desc(v[6], v[7]);
+  cas_desc(v[2], v[4]); cas_desc(v[3], v[5]);
+  cas_desc(v[1], v[4]); cas_desc(v[3], v[6]);
+  cas_desc(v[1], v[2]); cas_desc(v[3], v[4]); cas_desc(v[5], v[6]);
+}
+
+// L <- the KL largest of L and B, both descending: elementwise max against
+// the reversed B is bitonic and holds them; a bitonic merger sorts it.
+template <int KL>
+__device__ __forceinline__ void merge_desc(float (&L)[KL], const float (&B)[KL]) {
+#pragma unroll
+  for (int i = 0; i < KL; ++i) L[i] = fmaxf(L[i], B[KL - 1 - i]);
+#pragma unroll
+  for (int d = KL / 2; d >= 1; d /= 2) {
+#pragma unroll
+    for (int i = 0; i < KL; ++i)
+      if ((i & d) == 0) cas_desc(L[i], L[i + d]);
   }
 }
 
-// L[k] for a runtime k < KMAX; a compile-time index when KMAX == k + 1.
-template <int KMAX, bool EXACT>
-__device__ __forceinline__ float pick(const float (&L)[KMAX], int k) {
-  if constexpr (EXACT) {
-    return L[KMAX - 1];
+// Merge a block of 8 values into the descending list L (KL >= 8).
+template <int KL>
+__device__ __forceinline__ void merge_block8(float (&L)[KL], float (&v)[8]) {
+  sort8_desc(v);
+  float B[KL];
+#pragma unroll
+  for (int i = 0; i < KL; ++i) B[i] = i < 8 ? v[i] : -INFINITY;
+  merge_desc<KL>(L, B);
+}
+
+// Merge the partner lane's list (lane ^ 16) into L.
+template <int KL>
+__device__ __forceinline__ void merge_partner(float (&L)[KL]) {
+  float P[KL];
+#pragma unroll
+  for (int i = 0; i < KL; ++i) P[i] = __shfl_xor_sync(0xffffffffu, L[i], 16);
+  merge_desc<KL>(L, P);
+}
+
+// L[k]: a compile-time index when K1 = k + 1 is known, else a select chain.
+template <int KL, int K1>
+__device__ __forceinline__ float pick(const float (&L)[KL], int k) {
+  if constexpr (K1 > 0) {
+    return L[K1 - 1];
   } else {
     float a = L[0];
 #pragma unroll
-    for (int t = 1; t < KMAX; ++t) a = (t == k) ? L[t] : a;
+    for (int t = 1; t < KL; ++t) a = (t == k) ? L[t] : a;
     return a;
   }
 }
@@ -221,8 +272,9 @@ __device__ __forceinline__ uint32_t lut_load(const uint8_t* lut, uint32_t bin) {
   return lut[bin];
 }
 
-template <int E, int KMAX, bool EXACT, typename T, int MODE, int TILE>
+template <int E, int KL, int K1, typename T, int MODE, int TILE>
 __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kernel(const Args a) {
+  static_assert(TILE == 16, "phase B pairs two lanes per token of a 16-token tile");
   using GE = Geo<E, TILE>;
   using SM = Smem<E, T, MODE, TILE>;
   constexpr int NW = SM::NW;
@@ -300,7 +352,7 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
 
     // ---- phase A: scores in place, group maxima
     bool ext = false;
-#pragma unroll 1
+#pragma unroll kUnrollA
     for (int st = 0; st < GE::STEPS; ++st) {
       const int f = st * 256 + 8 * lane;
       const int row = f / E;
@@ -328,63 +380,140 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
     }
     const bool tile_ext = __any_sync(0xffffffffu, ext);
 
-    // ---- phase B: one lane per token, alpha and the top-k set
-    if (lane < rows) {
-      float gm[GE::G];
+    // ---- phase B: two lanes per token (lane & 15 = token, lane >> 4 = half).
+    // tau: each lane takes the top KL of its half of the group maxima, the
+    // pair merges.  alpha: the candidate groups (max >= tau) are dealt out by
+    // rank parity; each lane merges its groups' sorted values, the pair merges.
+    {
+      constexpr int GH = GE::G / 2;
+      const int t = lane & 15;
+      const int h = lane >> 4;
+      const bool actB = t < rows;
+      float gm[GH];
 #pragma unroll
-      for (int q = 0; q < GE::G / 4; ++q) {
-        const float4 v4 = reinterpret_cast<const float4*>(gmax + lane * GE::GP)[q];
-        gm[4 * q] = v4.x; gm[4 * q + 1] = v4.y; gm[4 * q + 2] = v4.z; gm[4 * q + 3] = v4.w;
-      }
-      float L[KMAX];
+      for (int g = 0; g < GH; ++g) gm[g] = actB ? gmax[t * GE::GP + h * GH + g] : -INFINITY;
+      float L[KL];
 #pragma unroll
-      for (int t = 0; t < KMAX; ++t) L[t] = -INFINITY;
+      for (int i = 0; i < KL; ++i) L[i] = -INFINITY;
+      if constexpr (GH % 8 == 0) {
 #pragma unroll
-      for (int g = 0; g < GE::G; ++g) insert_desc<KMAX>(L, gm[g]);
-      const float tau = pick<KMAX, EXACT>(L, k);
-      uint64_t mask = 0;
+        for (int b0 = 0; b0 < GH; b0 += 8) {
+          float v8[8];
 #pragma unroll
-      for (int g = 0; g < GE::G; ++g) mask |= (gm[g] >= tau ? 1ull : 0ull) << g;
-#pragma unroll
-      for (int t = 0; t < KMAX; ++t) L[t] = -INFINITY;
-      for (uint64_t mm = mask; mm; mm &= mm - 1) {
-        const int g = __ffsll((long long)mm) - 1;
-        float s8[8], b8[8];
-        load8(sc + lane * E + 8 * g, s8);
-        load8(bias_s + 8 * g, b8);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float v0, v1;
-          f2_unpack(f2_add(f2_pack(s8[2 * i], s8[2 * i + 1]), f2_pack(b8[2 * i], b8[2 * i + 1])),
-                    v0, v1);
-          insert_desc<KMAX>(L, v0);
-          insert_desc<KMAX>(L, v1);
+          for (int i = 0; i < 8; ++i) v8[i] = gm[b0 + i];
+          merge_block8<KL>(L, v8);
         }
-      }
-      const float alpha = pick<KMAX, EXACT>(L, k);
-      alpha_s[lane] = alpha;
-      const int64_t tok = t0 + lane;
-      if (a.alpha_out) a.alpha_out[tok] = alpha;
-      if (a.topk_out) {
-        int c_gt = 0;
+      } else {
 #pragma unroll
-        for (int t = 0; t < KMAX; ++t) c_gt += (t < k && L[t] > alpha) ? 1 : 0;
-        int ties = k - c_gt;
-        int c = 0;
-        int32_t* out = a.topk_out + tok * k;
-        for (uint64_t mm = mask; mm; mm &= mm - 1) {
-          const int g = __ffsll((long long)mm) - 1;
+        for (int g = 0; g < GH; ++g) insert_desc<KL>(L, gm[g]);
+      }
+      merge_partner<KL>(L);
+      const float tau = pick<KL, K1>(L, k);
+      uint32_t own = 0;
+#pragma unroll
+      for (int g = 0; g < GH; ++g) own |= (gm[g] >= tau ? 1u : 0u) << g;
+      own = actB ? own : 0u;
+      const uint32_t oth = __shfl_xor_sync(0xffffffffu, own, 16);
+      const uint64_t cand = h ? (((uint64_t)own << GH) | oth) : (((uint64_t)oth << GH) | own);
+#pragma unroll
+      for (int i = 0; i < KL; ++i) L[i] = -INFINITY;
+      const float* srow = sc + t * E;
+      for (uint64_t m = cand; m;) {
+        const int g0 = __ffsll((long long)m) - 1;
+        m &= m - 1;
+        int g1 = -1;
+        if (m) {
+          g1 = __ffsll((long long)m) - 1;
+          m &= m - 1;
+        }
+        const int g = h ? g1 : g0;
+        if (g >= 0) {
           float s8[8], b8[8];
-          load8(sc + lane * E + 8 * g, s8);
+          load8(srow + 8 * g, s8);
           load8(bias_s + 8 * g, b8);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float v = __fadd_rn(s8[i], b8[i]);
-            const bool take = (v > alpha) || (v == alpha && ties > 0);
-            if (take) {
-              if (!(v > alpha)) --ties;
-              out[c++] = 8 * g + i;
+          for (int i = 0; i < 4; ++i)
+            f2_unpack(f2_add(f2_pack(s8[2 * i], s8[2 * i + 1]), f2_pack(b8[2 * i], b8[2 * i + 1])),
+                      s8[2 * i], s8[2 * i + 1]);
+          merge_block8<KL>(L, s8);
+        }
+      }
+      merge_partner<KL>(L);
+      const float alpha = pick<KL, K1>(L, k);
+      const int64_t tok = t0 + t;
+      if (actB && h == 0) {
+        alpha_s[t] = alpha;
+        if (a.alpha_out) a.alpha_out[tok] = alpha;
+      }
+      if (a.topk_out) {
+        // experts with v > alpha, then ties at alpha by ascending index
+        int c_gt = 0;
+#pragma unroll
+        for (int i = 0; i < KL; ++i) c_gt += (i < k && L[i] > alpha) ? 1 : 0;
+        const int ties = k - c_gt;
+        int32_t* out = a.topk_out + tok * k;
+        if (__any_sync(0xffffffffu, actB && ties > 0)) {
+          // rare: a tie at alpha; one lane per token scans in index order
+          if (actB && h == 0) {
+            int tl = ties, c = 0;
+            for (uint64_t m = cand; m; m &= m - 1) {
+              const int g = __ffsll((long long)m) - 1;
+              float s8[8], b8[8];
+              load8(srow + 8 * g, s8);
+              load8(bias_s + 8 * g, b8);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float v = __fadd_rn(s8[i], b8[i]);
+                if (v > alpha || (v == alpha && tl > 0)) {
+                  if (!(v > alpha)) --tl;
+                  out[c++] = 8 * g + i;
+                }
+              }
             }
+          }
+        } else {
+          // the k experts above alpha: each lane writes its own from one end
+          // of the token's list in shared memory, then one lane sorts them
+          int32_t* lst = reinterpret_cast<int32_t*>(gmax) + t * 16;
+          int c = 0;
+          for (uint64_t m = cand; m;) {
+            const int g0 = __ffsll((long long)m) - 1;
+            m &= m - 1;
+            int g1 = -1;
+            if (m) {
+              g1 = __ffsll((long long)m) - 1;
+              m &= m - 1;
+            }
+            const int g = h ? g1 : g0;
+            if (g >= 0) {
+              float s8[8], b8[8];
+              load8(srow + 8 * g, s8);
+              load8(bias_s + 8 * g, b8);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                if (__fadd_rn(s8[i], b8[i]) > alpha) {
+                  lst[h ? k - 1 - c : c] = 8 * g + i;
+                  ++c;
+                }
+              }
+            }
+          }
+          __syncwarp();
+          if (actB && h == 0) {
+            int v[KL];
+#pragma unroll
+            for (int i = 0; i < KL; ++i) v[i] = i < k ? lst[i] : INT_MAX;
+#pragma unroll
+            for (int i = 0; i < KL; ++i)
+#pragma unroll
+              for (int j = KL - 1; j > i; --j) {
+                const int lo = min(v[j - 1], v[j]);
+                v[j] = max(v[j - 1], v[j]);
+                v[j - 1] = lo;
+              }
+#pragma unroll
+            for (int i = 0; i < KL; ++i)
+              if (i < k) out[i] = v[i];
           }
         }
       }
@@ -489,11 +618,11 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
   }
 }
 
-template <int E, int KMAX, bool EXACT, typename T, int MODE, int TILE>
+template <int E, int KL, int K1, typename T, int MODE, int TILE>
 int launch_one(const Args& a, cudaStream_t stream) {
   using SM = Smem<E, T, MODE, TILE>;
   static_assert(SM::NW >= 1, "tile does not fit shared memory");
-  auto kern = route_kernel<E, KMAX, EXACT, T, MODE, TILE>;
+  auto kern = route_kernel<E, KL, K1, T, MODE, TILE>;
   static bool attr_set = false;  // per instantiation; benign race (idempotent)
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kTotal) !=
@@ -514,10 +643,10 @@ template <int MODE, typename T, int TILE>
 int dispatch_E(int E, int k, const Args& a, cudaStream_t st) {
 #define QB_CASE(EE)                                                       \
   case EE:                                                                \
-    if (k + 1 == 7) return launch_one<EE, 7, true, T, MODE, TILE>(a, st); \
-    if (k + 1 == 9) return launch_one<EE, 9, true, T, MODE, TILE>(a, st); \
-    if (k + 1 <= 8) return launch_one<EE, 8, false, T, MODE, TILE>(a, st); \
-    return launch_one<EE, 16, false, T, MODE, TILE>(a, st);
+    if (k + 1 == 7) return launch_one<EE, 8, 7, T, MODE, TILE>(a, st);   \
+    if (k + 1 == 9) return launch_one<EE, 16, 9, T, MODE, TILE>(a, st);  \
+    if (k + 1 <= 8) return launch_one<EE, 8, 0, T, MODE, TILE>(a, st);   \
+    return launch_one<EE, 16, 0, T, MODE, TILE>(a, st);
   switch (E) {
     QB_CASE(32)
     QB_CASE(64)
@@ -531,7 +660,7 @@ int dispatch_E(int E, int k, const Args& a, cudaStream_t st) {
 }
 
 #ifndef QB_ROUTE_TILE
-#define QB_ROUTE_TILE 32
+#define QB_ROUTE_TILE 16
 #endif
 
 template <int MODE>

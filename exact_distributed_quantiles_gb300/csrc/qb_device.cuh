@@ -147,11 +147,15 @@ __device__ __forceinline__ f2_t sigmoid2_fast(f2_t X) {
   return f2_fma(R, Y, Y);
 }
 
+__device__ __forceinline__ float max_abs8(const float (&x)[8]) {
+  const float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+  return fmaxf(m, fmaxf(fmaxf(fabsf(x[4]), fabsf(x[5])), fmaxf(fabsf(x[6]), fabsf(x[7]))));
+}
+
 // Eight inputs in registers -> eight scores; the fast path when all |x| are
 // small enough, the exact scalar path otherwise.  Returns max |x|.
 __device__ __forceinline__ float sigmoid8(const float (&x)[8], float (&s)[8]) {
-  float m = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-  m = fmaxf(m, fmaxf(fmaxf(fabsf(x[4]), fabsf(x[5])), fmaxf(fabsf(x[6]), fabsf(x[7]))));
+  const float m = max_abs8(x);
   if (m <= kFastAbsX) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) f2_unpack(sigmoid2_fast(f2_pack(x[2 * i], x[2 * i + 1])),

@@ -17,104 +17,99 @@ namespace {
 // ------------------------------------------------------------------------
 // Lo-byte histogram from stored keys.
 //
-// Each lane owns 8 consecutive experts (one 16-byte chunk of a key row); the
-// selected hi byte of those experts sits in registers.  Matching keys are
-// counted in a per-CTA shared histogram of 16-bit counters packed in pairs
-// (two experts per 32-bit word), flushed with one global atomic per non-zero
-// counter.  A CTA flushes at least every 65535 rows so no counter wraps.
-// Pair-word layout: word(lo, p) = lo * (E/2) + (p & 3) * (E/8) + (p >> 2) with
-// p = e/2, so for a fixed element index the 32 lanes hit 32 distinct banks.
+// Work split: a CTA owns a column slice of 32 experts (64 bytes of every key
+// row) over a range of tokens, so its shared histogram is only 32 x 256 int32
+// counters and the flush issues few global atomics (merging 152 full
+// per-SM histograms through L2 atomics would cost more than the pass itself).
+// Four lanes cover one row slice (16 bytes = 8 keys each), a warp covers 8
+// rows per load; loads are double-buffered in registers.  Every key issues one
+// shared atomic: a key whose hi byte is not the selected one goes to a
+// per-lane dummy slot that is never flushed, so lanes never branch on their
+// own matches.  Layout: counter (e, lo) at word e * 257 + lo (257 spreads the
+// experts over the banks); dummies at 32 * 257 + j * 32 + lane.
 // ------------------------------------------------------------------------
-constexpr int kLoThreads = 1024;
-constexpr int kLoEpochRows = 65535;
+constexpr int kLoThreads = 256;
+constexpr int kLoEG = 32;                // experts per CTA slice
+constexpr int kLoRowW = 257;             // words per expert row in shared memory
+constexpr int kLoSmemWords = kLoEG * kLoRowW + 8 * 32;
 
-template <int E>
-__device__ __forceinline__ int lo_word(int lo, int e) {
-  const int p = e >> 1;
-  return lo * (E / 2) + (p & 3) * (E / 8) + (p >> 2);
+__device__ __forceinline__ void red_shared(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-template <int E>
-__global__ void __launch_bounds__(kLoThreads, 1)
-    keys_hist_lo_kernel(const uint16_t* __restrict__ keys, int64_t N,
+__global__ void __launch_bounds__(kLoThreads)
+    keys_hist_lo_kernel(const uint16_t* __restrict__ keys, int64_t N, int E,
                         const int32_t* __restrict__ sel, int32_t* __restrict__ hist_lo,
                         int64_t rows_per_cta) {
-  static_assert(E <= 256, "shared lo histogram sized for E <= 256");
-  extern __shared__ __align__(16) uint32_t h[];
-  constexpr int kWords = 256 * E / 2;
+  __shared__ uint32_t h[kLoSmemWords];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   constexpr int kWarps = kLoThreads / 32;
-  // 32 chunks of 8 keys = 256 elements per warp step; E <= 256 divides it.
-  const int e0 = (8 * lane) % E;
-  uint32_t pat[4], valid[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int s0 = sel[e0 + 2 * i], s1 = sel[e0 + 2 * i + 1];
-    pat[i] = ((uint32_t)(s0 & 0xFF) << 8) | ((uint32_t)(s1 & 0xFF) << 24);
-    valid[i] = (s0 >= 0 ? 1u : 0u) | (s1 >= 0 ? 2u : 0u);
-  }
-  const int64_t r_begin = (int64_t)blockIdx.x * rows_per_cta;
+  const int n_eg = E / kLoEG;
+  const int eg = blockIdx.x % n_eg;
+  const int64_t r_begin = (int64_t)(blockIdx.x / n_eg) * rows_per_cta;
   int64_t r_end = r_begin + rows_per_cta;
   if (r_end > N) r_end = N;
-  constexpr int kRowsPerStep = 256 / E;
-  for (int64_t ep = r_begin; ep < r_end; ep += kLoEpochRows) {
-    const int64_t ep_end = (ep + kLoEpochRows < r_end) ? ep + kLoEpochRows : r_end;
-    for (int i = threadIdx.x; i < kWords; i += kLoThreads) h[i] = 0;
-    __syncthreads();
-    // flat element range of this epoch, in 256-element warp steps
-    const int64_t f_begin = ep * E, f_end = ep_end * E;
-    const int64_t steps = (f_end - f_begin + 255) / 256;
-    constexpr int kU = 4;  // 16-byte chunks in flight per lane
-    for (int64_t st0 = (int64_t)warp * kU; st0 < steps; st0 += (int64_t)kWarps * kU) {
-      uint4 u[kU];
+  const int c4 = lane & 3;    // which 8-key chunk of the 32-expert slice
+  const int rsub = lane >> 2; // row within the warp's 8 rows
+  const int el0 = 8 * c4;     // first local expert of this lane
+  for (int i = threadIdx.x; i < kLoSmemWords; i += kLoThreads) h[i] = 0;
+  // selected hi byte of each key pair, at the pair's hi-byte positions
+  uint32_t spat[4];
 #pragma unroll
-      for (int q = 0; q < kU; ++q) {
-        const int64_t f = f_begin + (st0 + q) * 256 + 8 * lane;
-        u[q] = (f < f_end) ? __ldcs(reinterpret_cast<const uint4*>(keys + f))
-                           : make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
-      }
+  for (int i = 0; i < 4; ++i)
+    spat[i] = ((uint32_t)(sel[eg * kLoEG + el0 + 2 * i] & 0xFF) << 8) |
+              ((uint32_t)(sel[eg * kLoEG + el0 + 2 * i + 1] & 0xFF) << 24);
+  const uint32_t hb = (uint32_t)__cvta_generic_to_shared(h);
+  uint32_t ebase[8], dummy[8];
 #pragma unroll
-      for (int q = 0; q < kU; ++q) {
-        const int64_t f = f_begin + (st0 + q) * 256 + 8 * lane;
-        if (f >= f_end) continue;
-        const uint32_t w[4] = {u[q].x, u[q].y, u[q].z, u[q].w};
+  for (int j = 0; j < 8; ++j) {
+    ebase[j] = hb + 4u * (uint32_t)((el0 + j) * kLoRowW);
+    dummy[j] = hb + 4u * (uint32_t)(kLoEG * kLoRowW + j * 32 + lane);
+  }
+  __syncthreads();
+
+  const int64_t n_rows = r_end > r_begin ? r_end - r_begin : 0;
+  const uint16_t* base = keys + r_begin * E + eg * kLoEG + el0;
+  constexpr int kU = 4;                           // 8-row blocks per warp in flight
+  const int64_t stride = (int64_t)kWarps * 8 * kU;  // rows per CTA iteration
+  uint4 cur[kU];
+  int64_t r0 = (int64_t)warp * 8 * kU + rsub;
+#pragma unroll
+  for (int q = 0; q < kU; ++q) {
+    const int64_t r = r0 + 8 * q;
+    cur[q] = r < n_rows ? __ldcs(reinterpret_cast<const uint4*>(base + r * E))
+                        : make_uint4(0u, 0u, 0u, 0u);
+  }
+  for (; r0 < n_rows; r0 += stride) {
+    uint4 nxt[kU];
+#pragma unroll
+    for (int q = 0; q < kU; ++q) {
+      const int64_t r = r0 + stride + 8 * q;
+      nxt[q] = r < n_rows ? __ldcs(reinterpret_cast<const uint4*>(base + r * E))
+                          : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int q = 0; q < kU; ++q) {
+      if (r0 + 8 * q < n_rows) {
+        const uint32_t w[4] = {cur[q].x, cur[q].y, cur[q].z, cur[q].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const uint32_t x = w[i] ^ pat[i];
-          const bool m0 = ((x & 0x0000FF00u) == 0u) && (valid[i] & 1u);
-          const bool m1 = ((x & 0xFF000000u) == 0u) && (valid[i] & 2u);
-          if (m0) atomicAdd(&h[lo_word<E>(w[i] & 0xFF, e0 + 2 * i)], 1u);
-          if (m1) atomicAdd(&h[lo_word<E>((w[i] >> 16) & 0xFF, e0 + 2 * i + 1)], 0x10000u);
+          const uint32_t x = w[i] ^ spat[i];  // selected hi bytes become 0
+          const uint32_t a0 = ebase[2 * i] + 4u * (w[i] & 0xFFu);
+          const uint32_t a1 = ebase[2 * i + 1] + 4u * ((w[i] >> 16) & 0xFFu);
+          red_shared((x & 0x0000FF00u) ? dummy[2 * i] : a0, 1u);
+          red_shared((x & 0xFF000000u) ? dummy[2 * i + 1] : a1, 1u);
         }
       }
+      cur[q] = nxt[q];
     }
-    (void)kRowsPerStep;
-    __syncthreads();
-    for (int i = threadIdx.x; i < kWords; i += kLoThreads) {
-      const uint32_t c = h[i];
-      if (c) {
-        const int lo = i / (E / 2);
-        const int q = i % (E / 2);
-        const int p = (q % (E / 8)) * 4 + q / (E / 8);  // inverse of the pair permutation
-        if (c & 0xFFFFu) atomicAdd(hist_lo + (int64_t)(2 * p) * 256 + lo, (int)(c & 0xFFFFu));
-        if (c >> 16) atomicAdd(hist_lo + (int64_t)(2 * p + 1) * 256 + lo, (int)(c >> 16));
-      }
-    }
-    __syncthreads();
   }
-}
-
-// E = 512: no shared privatisation (the packed histogram would need 256 KB).
-__global__ void keys_hist_lo_global_kernel(const uint16_t* __restrict__ keys, int64_t N, int E,
-                                           const int32_t* __restrict__ sel,
-                                           int32_t* __restrict__ hist_lo) {
-  const int64_t total = N * (int64_t)E;
-  for (int64_t f = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; f < total;
-       f += (int64_t)gridDim.x * blockDim.x) {
-    const int e = (int)(f % E);
-    const uint32_t key = keys[f];
-    if ((int32_t)(key >> 8) == sel[e]) atomicAdd(hist_lo + (int64_t)e * 256 + (key & 0xFF), 1);
+  __syncthreads();
+  for (int i = threadIdx.x; i < kLoEG * 256; i += kLoThreads) {
+    const int el = i >> 8, lo = i & 255;
+    const uint32_t c = h[el * kLoRowW + lo];
+    if (c) atomicAdd(hist_lo + (int64_t)(eg * kLoEG + el) * 256 + lo, (int)c);
   }
 }
 
@@ -203,19 +198,62 @@ __global__ void __launch_bounds__(256) eqb_lo_select_kernel(
   }
 }
 
-__global__ void __launch_bounds__(512) eqb_center_kernel(float* __restrict__ bias_out, int E) {
-  __shared__ float q_s[512];
-  __shared__ double mu_s;
-  for (int j = threadIdx.x; j < E; j += blockDim.x) q_s[j] = bias_out[j];
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double sum = 0.0;
-    for (int j = 0; j < E; ++j) sum = __dadd_rn(sum, (double)q_s[j]);
-    mu_s = __ddiv_rn(sum, (double)E);
+// Sum of E <= 512 bf16-valued fp32 numbers in fp64, equal to the ascending
+// serial fp64 sum.  When the non-zero values' binary exponents span at most
+// 36, every partial sum in any order is exact (8 significant bits per value,
+// 1 + 9 more for the magnitude of up to 512 terms: 36 + 17 <= 53 bits), so a
+// parallel tree gives the serial result; otherwise one thread sums serially.
+__device__ double bf16_values_sum_fp64(const float* q_s, int E, double* red, int* emin_s,
+                                       int* emax_s, int* bad_s) {
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    *emin_s = 1 << 20;
+    *emax_s = -(1 << 20);
+    *bad_s = 0;
   }
   __syncthreads();
+  for (int j = tid; j < E; j += blockDim.x) {
+    const uint32_t u = __float_as_uint(q_s[j]);
+    const int ex = (int)((u >> 23) & 0xFFu);
+    if (ex == 0xFF) atomicOr(bad_s, 1);
+    if ((u & 0x7FFFFFFFu) != 0) {
+      atomicMin(emin_s, ex);
+      atomicMax(emax_s, ex);
+    }
+  }
+  __syncthreads();
+  const bool tree = (*bad_s == 0) && (*emax_s - *emin_s <= 36);
+  double v = 0.0;
+  if (tree) {
+    for (int j = tid; j < E; j += blockDim.x) v = __dadd_rn(v, (double)q_s[j]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v = __dadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if ((tid & 31) == 0) red[tid >> 5] = v;
+    __syncthreads();
+    if (tid == 0) {
+      double s = 0.0;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s = __dadd_rn(s, red[w]);
+      red[0] = s;
+    }
+  } else if (tid == 0) {
+    double s = 0.0;
+    for (int j = 0; j < E; ++j) s = __dadd_rn(s, (double)q_s[j]);
+    red[0] = s;
+  }
+  __syncthreads();
+  return red[0];
+}
+
+__global__ void __launch_bounds__(512) eqb_center_kernel(float* __restrict__ bias_out, int E) {
+  __shared__ float q_s[512];
+  __shared__ double red[16];
+  __shared__ int emin_s, emax_s, bad_s;
+  for (int j = threadIdx.x; j < E; j += blockDim.x) q_s[j] = bias_out[j];
+  __syncthreads();
+  const double mu = __ddiv_rn(bf16_values_sum_fp64(q_s, E, red, &emin_s, &emax_s, &bad_s),
+                              (double)E);
   for (int j = threadIdx.x; j < E; j += blockDim.x)
-    bias_out[j] = __double2float_rn(__dsub_rn((double)q_s[j], mu_s));
+    bias_out[j] = __double2float_rn(__dsub_rn((double)q_s[j], mu));
 }
 
 // First index where the inclusive prefix sum of the row reaches `target`, or
@@ -341,40 +379,19 @@ __global__ void sigmoid_kernel(const float* __restrict__ x, float* __restrict__ 
 
 int launch_keys_hist_lo(const uint16_t* keys, int64_t N, int E, const int32_t* sel,
                         int32_t* hist_lo, cudaStream_t stream) {
-  if (E == 512) {
-    int64_t grid = (int64_t)sm_count() * 8;
-    keys_hist_lo_global_kernel<<<(unsigned)grid, 256, 0, stream>>>(keys, N, E, sel, hist_lo);
-    return launch_status();
+  if (E < kLoEG) {  // E = 32 is one slice already; smaller E is not supported
+    if (E != 32) return QB_EUNSUPPORTED;
   }
-  const int64_t ctas_max = sm_count();
-  // at least 32 rows per CTA so that flush work stays small against the pass
-  int64_t ctas = (N + 31) / 32;
-  if (ctas > ctas_max) ctas = ctas_max;
-  if (ctas < 1) ctas = 1;
-  const int64_t rows_per_cta = (N + ctas - 1) / ctas;
-#define QB_LO(EE)                                                                            \
-  case EE: {                                                                                 \
-    const int smem = 256 * EE / 2 * 4;                                                       \
-    static bool attr = false;                                                                \
-    if (!attr) {                                                                             \
-      if (cudaFuncSetAttribute(keys_hist_lo_kernel<EE>,                                      \
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) \
-        return launch_status();                                                              \
-      attr = true;                                                                           \
-    }                                                                                        \
-    keys_hist_lo_kernel<EE><<<(unsigned)ctas, kLoThreads, smem, stream>>>(keys, N, sel, hist_lo, \
-                                                                          rows_per_cta);     \
-    return launch_status();                                                                  \
-  }
-  switch (E) {
-    QB_LO(32)
-    QB_LO(64)
-    QB_LO(128)
-    QB_LO(256)
-    default:
-      return QB_EUNSUPPORTED;
-  }
-#undef QB_LO
+  const int n_eg = E / kLoEG;
+  // about four CTAs per SM, at least 64 rows per CTA
+  int64_t n_tr = ((int64_t)sm_count() * 4 + n_eg - 1) / n_eg;
+  const int64_t max_tr = (N + 63) / 64;
+  if (n_tr > max_tr) n_tr = max_tr;
+  if (n_tr < 1) n_tr = 1;
+  const int64_t rows_per_cta = (N + n_tr - 1) / n_tr;
+  keys_hist_lo_kernel<<<(unsigned)(n_tr * n_eg), kLoThreads, 0, stream>>>(keys, N, E, sel, hist_lo,
+                                                                        rows_per_cta);
+  return launch_status();
 }
 
 int launch_select_hi(const int32_t* hist_hi, int E, int64_t r, int32_t* sel, int32_t* r_lo,

@@ -9,49 +9,64 @@
 // rho = tanh(rho_raw) - mean_e tanh(rho_raw).
 //
 // Two kernels:
-//   lei_rho_kernel    one CTA per local batch: load counts in shared memory,
-//                     rho in fp64, c_e = RN32(eta * rho_e) into the caller's
-//                     workspace [num_batches, E];
+//   lei_rho_kernel    one 8-CTA cluster per local batch: load counts in
+//                     shared memory, reduced over the cluster, rho in fp64,
+//                     c_e = RN32(eta * rho_e) into the caller's workspace
+//                     [num_batches, E];
 //   lei_apply_kernel  grid-stride stream over grad in 16-byte chunks:
 //                     grad += c_e of the chunk's batch (c rows stay in L1/L2).
+#include <cooperative_groups.h>
+
 #include "qb_device.cuh"
 #include "qb_internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace qb {
 namespace {
 
-constexpr int kRhoThreads = 1024;
+constexpr int kRhoCluster = 8;  // CTAs per local batch (one thread-block cluster)
+constexpr int kRhoThreads = 512;
 constexpr int kRhoWarps = kRhoThreads / 32;
 
-// One CTA per local batch.  Top-k entries are read 16 at a time per thread
-// (four 16-byte loads in flight) and counted in per-warp shared histograms,
-// which are summed at the end.
-__global__ void __launch_bounds__(kRhoThreads) lei_rho_kernel(const int32_t* __restrict__ topk,
-                                                              int64_t N, int E, int k, float eta,
-                                                              int64_t batch_tokens,
-                                                              float* __restrict__ ws) {
+// One cluster of 8 CTAs per local batch.  Each CTA counts one eighth of the
+// batch's top-k entries (16-byte loads, four in flight per thread) into
+// per-warp shared histograms and reduces them to its own count row; after a
+// cluster barrier, CTA 0 sums the eight rows through distributed shared
+// memory, computes rho in fp64 and writes c_e = RN32(eta * rho_e).  A second
+// cluster barrier keeps every row alive until CTA 0 has read it.
+__global__ void __cluster_dims__(kRhoCluster, 1, 1) __launch_bounds__(kRhoThreads)
+    lei_rho_kernel(const int32_t* __restrict__ topk, int64_t N, int E, int k, float eta,
+                   int64_t batch_tokens, float* __restrict__ ws) {
+  cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ int32_t sub[];  // [kRhoWarps][E]
+  __shared__ int32_t cnt[512];
+  __shared__ double red[kRhoWarps];
   __shared__ double t_s[512];
-  __shared__ double mean_s;
   const int warp = threadIdx.x >> 5;
-  const int64_t b = blockIdx.x;
+  const int rank = (int)cluster.block_rank();
+  const int64_t b = blockIdx.x / kRhoCluster;
   const int64_t i0 = b * batch_tokens;
   int64_t i1 = i0 + batch_tokens;
   if (i1 > N) i1 = N;
   for (int q = threadIdx.x; q < kRhoWarps * E; q += blockDim.x) sub[q] = 0;
   __syncthreads();
   int32_t* mine = sub + warp * E;
-  const int64_t n_idx = (i1 - i0) * k;
-  const int32_t* t = topk + i0 * k;
+  const int64_t n_all = (i1 - i0) * k;
+  const int64_t per = ((n_all + kRhoCluster - 1) / kRhoCluster + 3) & ~(int64_t)3;
+  const int64_t s0 = rank * per < n_all ? rank * per : n_all;
+  const int64_t s1 = s0 + per < n_all ? s0 + per : n_all;
+  const int32_t* t = topk + i0 * k + s0;
+  const int64_t n_idx = s1 - s0;
   // scalar head until 16-byte alignment, then int4 body, then scalar tail
   const int64_t head = ((16 - (reinterpret_cast<uintptr_t>(t) & 15)) & 15) / 4;
-  const int64_t h = head < n_idx ? head : n_idx;
-  for (int64_t q = threadIdx.x; q < h; q += blockDim.x) {
+  const int64_t hd = head < n_idx ? head : n_idx;
+  for (int64_t q = threadIdx.x; q < hd; q += blockDim.x) {
     const int32_t e = t[q];
     if ((unsigned)e < (unsigned)E) atomicAdd(&mine[e], 1);
   }
-  const int4* t4 = reinterpret_cast<const int4*>(t + h);
-  const int64_t n4 = (n_idx - h) / 4;
+  const int4* t4 = reinterpret_cast<const int4*>(t + hd);
+  const int64_t n4 = (n_idx - hd) / 4;
   constexpr int kU = 4;
   for (int64_t q0 = threadIdx.x; q0 < n4; q0 += (int64_t)blockDim.x * kU) {
     int4 v[kU];
@@ -68,26 +83,41 @@ __global__ void __launch_bounds__(kRhoThreads) lei_rho_kernel(const int32_t* __r
         if ((unsigned)ev[c] < (unsigned)E) atomicAdd(&mine[ev[c]], 1);
     }
   }
-  for (int64_t q = h + 4 * n4 + threadIdx.x; q < n_idx; q += blockDim.x) {
+  for (int64_t q = hd + 4 * n4 + threadIdx.x; q < n_idx; q += blockDim.x) {
     const int32_t e = t[q];
     if ((unsigned)e < (unsigned)E) atomicAdd(&mine[e], 1);
   }
   __syncthreads();
-  const double T = __ddiv_rn((double)((i1 - i0) * (int64_t)k), (double)E);
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int32_t load = 0;
-    for (int w = 0; w < kRhoWarps; ++w) load += sub[w * E + e];
-    t_s[e] = tanh(__ddiv_rn(__dsub_rn((double)load, T), T));
+    int32_t c = 0;
+    for (int w = 0; w < kRhoWarps; ++w) c += sub[w * E + e];
+    cnt[e] = c;
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
+  cluster.sync();
+  if (rank == 0) {
+    const double T = __ddiv_rn((double)((i1 - i0) * (int64_t)k), (double)E);
+    double part = 0.0;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int32_t load = 0;
+#pragma unroll
+      for (int r = 0; r < kRhoCluster; ++r) load += cluster.map_shared_rank(cnt, r)[e];
+      t_s[e] = tanh(__ddiv_rn(__dsub_rn((double)load, T), T));
+      part = __dadd_rn(part, t_s[e]);
+    }
+    // mean of tanh over experts: a fixed-shape tree (differs from a serial
+    // sum only in the last bits of an fp64 value)
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) part = __dadd_rn(part, __shfl_xor_sync(0xffffffffu, part, o));
+    if ((threadIdx.x & 31) == 0) red[warp] = part;
+    __syncthreads();
     double sum = 0.0;
-    for (int e = 0; e < E; ++e) sum = __dadd_rn(sum, t_s[e]);
-    mean_s = __ddiv_rn(sum, (double)E);
+#pragma unroll
+    for (int w = 0; w < kRhoWarps; ++w) sum = __dadd_rn(sum, red[w]);
+    const double mean = __ddiv_rn(sum, (double)E);
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+      ws[b * E + e] = __double2float_rn(__dmul_rn((double)eta, __dsub_rn(t_s[e], mean)));
   }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x)
-    ws[b * E + e] = __double2float_rn(__dmul_rn((double)eta, __dsub_rn(t_s[e], mean_s)));
+  cluster.sync();
 }
 
 // grad += c[batch(row)] streamed in 16-byte chunks.  Each CTA walks whole
@@ -141,15 +171,8 @@ int launch_lei(float* grad, const int32_t* topk, int64_t N, int E, int k, float 
                int64_t batch_tokens, float* workspace, cudaStream_t stream) {
   const int64_t nb = (N + batch_tokens - 1) / batch_tokens;
   const int smem = kRhoWarps * E * (int)sizeof(int32_t);
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(lei_rho_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kRhoWarps * 512 * (int)sizeof(int32_t)) != cudaSuccess)
-      return launch_status();
-    attr = true;
-  }
-  lei_rho_kernel<<<(unsigned)nb, kRhoThreads, smem, stream>>>(topk, N, E, k, eta, batch_tokens,
-                                                             workspace);
+  lei_rho_kernel<<<(unsigned)(nb * kRhoCluster), kRhoThreads, smem, stream>>>(
+      topk, N, E, k, eta, batch_tokens, workspace);
   int st = launch_status();
   if (st != QB_OK) return st;
   int e4_log2 = 0;

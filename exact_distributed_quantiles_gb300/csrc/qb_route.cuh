@@ -14,7 +14,8 @@
 //
 // Work decomposition (one CTA per SM, NW warps, each warp independent):
 //   a warp owns a tile of TILE consecutive tokens held in shared memory,
-//   filled by cp.async.bulk (one mbarrier per warp);
+//   filled by cp.async.bulk in groups of rows, one mbarrier per row group, so
+//   that phase A waits only for the rows it is about to read;
 //   phase A  element-wise over the tile, 8 experts per lane: s = sigma(x)
 //            (packed f32x2 arithmetic) written back in place, v = s + b, the
 //            max of every group of 8 experts;
@@ -43,10 +44,6 @@ namespace route {
 constexpr int kWin = 32;      // hi-byte bins privatised in shared memory
 constexpr int kDummy = kWin;  // slot of every other bin (never flushed)
 constexpr int kSmemLimit = 227 * 1024;
-#ifndef QB_UNROLL_A
-#define QB_UNROLL_A 1
-#endif
-constexpr int kUnrollA = QB_UNROLL_A;  // phase-A steps unrolled (ILP)
 
 struct Args {
   const void* logits;
@@ -98,7 +95,9 @@ struct Smem {
   static constexpr int kTileBytes = TILE * E * 4;  // fp32 scores; bf16 input sits in the upper half
   static constexpr int kGmax = round16(TILE * (GE::GP > 16 ? GE::GP : 16) * 4);
   static constexpr int kAlpha = round16(TILE * 4);
-  static constexpr int kWarp = kTileBytes + kGmax + kAlpha + 16;  // + mbarrier
+  static constexpr int GR = (256 / E) > 4 ? 256 / E : 4;  // rows per load group
+  static constexpr int NGRP = TILE / GR;                   // mbarriers per warp
+  static constexpr int kWarp = kTileBytes + kGmax + kAlpha + round16(NGRP * 8);
   static constexpr int nw_fit() {
     int n = (kSmemLimit - kFixed) / kWarp;
     return n > 16 ? 16 : n;
@@ -222,6 +221,21 @@ __device__ __forceinline__ void issue_rows(unsigned char* tile, const T* logits,
            (uint32_t)((r1 - r0) * E * sizeof(T)), bar);
 }
 
+// Issue the load of every row group of the next tile that is complete inside
+// [0, nf) and not issued yet (groups below `issued`); one mbarrier per group.
+template <int E, typename T, int TILE, int GR>
+__device__ __forceinline__ void issue_groups(unsigned char* tile, const T* logits, int64_t start,
+                                             int nrows, int nf, int& issued, uint64_t* bars) {
+  while (issued * GR < nrows) {
+    const int r0 = issued * GR;
+    const int r1 = (r0 + GR < nrows) ? r0 + GR : nrows;
+    if (nf < r1) break;
+    mbar_arrive_expect_tx(bars + issued, (uint32_t)((r1 - r0) * E * sizeof(T)));
+    issue_rows<E, T, TILE>(tile, logits, start, r0, r1, bars + issued);
+    ++issued;
+  }
+}
+
 __device__ __forceinline__ void load8(const float* p, float (&x)[8]) {
   const float4 a = reinterpret_cast<const float4*>(p)[0];
   const float4 b = reinterpret_cast<const float4*>(p)[1];
@@ -247,15 +261,15 @@ __device__ __forceinline__ void store8(float* p, const float (&x)[8]) {
 // Eight margins alpha - s -> four packed key pairs.  `fold` maps margins that
 // round to bf16 -0 onto the +0 key; they only occur when some score is below
 // 2^-100 (a logit below -75), which phase A flags per tile.
-__device__ __forceinline__ void keys8(float alpha, const float (&s)[8], bool fold,
-                                      uint32_t (&kw)[4]) {
+template <bool FOLD>
+__device__ __forceinline__ void keys8(float alpha, const float (&s)[8], uint32_t (&kw)[4]) {
   const f2_t A = f2_splat(alpha);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     float r0, r1;
     f2_unpack(f2_sub(A, f2_pack(s[2 * i], s[2 * i + 1])), r0, r1);
     uint32_t w = bf16x2_rn(r0, r1);
-    if (fold) {
+    if constexpr (FOLD) {
       const uint32_t nz = (w & 0x7FFF7FFFu) + 0x7FFF7FFFu;
       w &= (nz | 0x7FFF7FFFu);
     }
@@ -289,7 +303,8 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
   float* sc = reinterpret_cast<float*>(tile);
   float* gmax = reinterpret_cast<float*>(wbase + SM::kTileBytes);
   float* alpha_s = reinterpret_cast<float*>(wbase + SM::kTileBytes + SM::kGmax);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(wbase + SM::kTileBytes + SM::kGmax + SM::kAlpha);
+  constexpr int GR = SM::GR;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(wbase + SM::kTileBytes + SM::kGmax + SM::kAlpha);
   const T* logits = static_cast<const T*>(a.logits);
   const int k = a.k;
 
@@ -300,7 +315,7 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
   }
   for (int i = threadIdx.x; i < E; i += blockDim.x) bias_s[i] = a.bias[i];
   if (lane == 0) {
-    mbar_init(bar, 1);
+    for (int q = 0; q < SM::NGRP; ++q) mbar_init(bars + q, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -335,8 +350,8 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
   if (tix < n_tiles && lane == 0) {
     const int64_t t0 = tix * TILE;
     const int rows = (int)((a.N - t0) < TILE ? (a.N - t0) : TILE);
-    mbar_arrive_expect_tx(bar, (uint32_t)(rows * E * sizeof(T)));
-    issue_rows<E, T, TILE>(tile, logits, t0, 0, rows, bar);
+    int issued = 0;
+    issue_groups<E, T, TILE, GR>(tile, logits, t0, rows, rows, issued, bars);
   }
 
   for (; tix < n_tiles && ok; tix += wstride) {
@@ -346,38 +361,69 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
     const int64_t n0 = nt * TILE;
     const int nrows = nt < n_tiles ? (int)((a.N - n0) < TILE ? (a.N - n0) : TILE) : 0;
 
-    ok = mbar_wait_bounded(bar, parity, a.status);
-    parity ^= 1u;
-    if (!ok) break;
 
-    // ---- phase A: scores in place, group maxima
+    // ---- phase A: scores in place, group maxima.  Two 8-element chunks per
+    // lane per iteration (all loads first, one fast/slow decision for both,
+    // then straight-line packed arithmetic) for instruction-level parallelism.
     bool ext = false;
-#pragma unroll kUnrollA
-    for (int st = 0; st < GE::STEPS; ++st) {
-      const int f = st * 256 + 8 * lane;
-      const int row = f / E;
-      const bool act = row < rows;
-      float x[8];
-      if (act) load8(x_ptr<E, T, TILE>(tile, f), x);
+    constexpr int NS = (GE::STEPS % 2 == 0) ? 2 : 1;
+#pragma unroll 1
+    for (int st0 = 0; st0 < GE::STEPS; st0 += NS) {
+      float x[NS][8];
+      bool act[NS];
+#pragma unroll
+      for (int u = 0; u < NS; ++u) {
+        const int st = st0 + u;
+        act[u] = (st * 256 + 8 * lane) / E < rows;
+        if ((st * 256) % (GR * E) == 0) {
+          const int q = (st * 256) / (GR * E);
+          if (q * GR < rows && !mbar_wait_bounded(bars + q, parity, a.status)) ok = false;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < NS; ++u)
+        if (act[u] && ok) load8(x_ptr<E, T, TILE>(tile, (st0 + u) * 256 + 8 * lane), x[u]);
       if constexpr (sizeof(T) != 4) __syncwarp();
-      if (act) {
-        float s[8];
-        const float m = sigmoid8(x, s);
-        ext |= m > kFoldAbsX;
+      float m = 0.0f;
+#pragma unroll
+      for (int u = 0; u < NS; ++u)
+        if (act[u]) m = fmaxf(m, max_abs8(x[u]));
+      ext |= m > kFoldAbsX;
+      float s[NS][8];
+      if (m <= kFastAbsX) {
+#pragma unroll
+        for (int u = 0; u < NS; ++u)
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            f2_unpack(sigmoid2_fast(f2_pack(x[u][2 * i], x[u][2 * i + 1])), s[u][2 * i],
+                      s[u][2 * i + 1]);
+      } else {
+#pragma unroll
+        for (int u = 0; u < NS; ++u)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) s[u][i] = sigmoid_pinned(x[u][i]);
+      }
+#pragma unroll
+      for (int u = 0; u < NS; ++u) {
+        if (!act[u]) continue;
+        const int st = st0 + u;
+        const int f = st * 256 + 8 * lane;
         const bool hi = (E == 512) && (st & 1);
         float v[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const f2_t B = hi ? f2_pack(breg[(8 + 2 * i) % GE::BREG], breg[(9 + 2 * i) % GE::BREG])
                             : f2_pack(breg[2 * i], breg[2 * i + 1]);
-          f2_unpack(f2_add(f2_pack(s[2 * i], s[2 * i + 1]), B), v[2 * i], v[2 * i + 1]);
+          f2_unpack(f2_add(f2_pack(s[u][2 * i], s[u][2 * i + 1]), B), v[2 * i], v[2 * i + 1]);
         }
         const float g = fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])),
                               fmaxf(fmaxf(v[4], v[5]), fmaxf(v[6], v[7])));
-        store8(sc + f, s);
-        gmax[row * GE::GP + ((f % E) >> 3)] = g;
+        store8(sc + f, s[u]);
+        gmax[(f / E) * GE::GP + ((f % E) >> 3)] = g;
       }
     }
+    parity ^= 1u;
+    if (!__all_sync(0xffffffffu, ok)) break;
     const bool tile_ext = __any_sync(0xffffffffu, ext);
 
     // ---- phase B: two lanes per token (lane & 15 = token, lane >> 4 = half).
@@ -390,8 +436,17 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
       const int h = lane >> 4;
       const bool actB = t < rows;
       float gm[GH];
+      if constexpr (GH % 4 == 0) {
 #pragma unroll
-      for (int g = 0; g < GH; ++g) gm[g] = actB ? gmax[t * GE::GP + h * GH + g] : -INFINITY;
+        for (int q = 0; q < GH / 4; ++q) {
+          const float4 v4 = actB ? reinterpret_cast<const float4*>(gmax + t * GE::GP + h * GH)[q]
+                                 : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+          gm[4 * q] = v4.x; gm[4 * q + 1] = v4.y; gm[4 * q + 2] = v4.z; gm[4 * q + 3] = v4.w;
+        }
+      } else {
+#pragma unroll
+        for (int g = 0; g < GH; ++g) gm[g] = actB ? gmax[t * GE::GP + h * GH + g] : -INFINITY;
+      }
       float L[KL];
 #pragma unroll
       for (int i = 0; i < KL; ++i) L[i] = -INFINITY;
@@ -521,8 +576,7 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
     __syncwarp();
 
     // ---- phase C: margins, keys, histograms; refill freed rows
-    if (lane == 0 && nrows > 0) mbar_arrive_expect_tx(bar, (uint32_t)(nrows * E * sizeof(T)));
-    int copied = 0;
+    int issued = 0;
 #pragma unroll 1
     for (int st = 0; st < GE::STEPS; ++st) {
       const int f = st * 256 + 8 * lane;
@@ -555,7 +609,10 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
         if (act) {
           float s[8];
           load8(sc + f, s);
-          keys8(alpha_s[row], s, tile_ext, kw);
+          if (tile_ext)
+            keys8<true>(alpha_s[row], s, kw);
+          else
+            keys8<false>(alpha_s[row], s, kw);
           if (MODE == kModeHi && a.keys_out)
             *reinterpret_cast<uint4*>(a.keys_out + tok * E + e0) =
                 make_uint4(kw[0], kw[1], kw[2], kw[3]);
@@ -593,12 +650,9 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
         }
       }
       __syncwarp();
-      if (lane == 0 && nrows > 0) {
-        int nf = rows_free<E, T, TILE>((st + 1) * 256);
-        nf = nf < nrows ? nf : nrows;
-        issue_rows<E, T, TILE>(tile, logits, n0, copied, nf, bar);
-        if (nf > copied) copied = nf;
-      }
+      if (lane == 0 && nrows > 0)
+        issue_groups<E, T, TILE, GR>(tile, logits, n0, nrows, rows_free<E, T, TILE>((st + 1) * 256),
+                                     issued, bars);
     }
   }
 

@@ -199,3 +199,14 @@ def test_full_step_layer_at_bench_size(qb, orc):
     ref = orc.eqb_global_batch([out.cpu().numpy()], bias.cpu().numpy(), w.k)
     _check_eqb(res, ref)
     assert np.array_equal(np_u16(res["keys"]), np.concatenate(ref["keys"]))
+
+
+@pytest.mark.parametrize("E,k", [(32, 1), (64, 6), (128, 8), (256, 6), (512, 15)])
+def test_eqb_all_expert_counts(qb, orc, E, k):
+    # the whole EQB chain (hi pass, select, lo pass from keys, finalize) for
+    # every supported expert count, several tiles and a ragged tail
+    w = inputs.scaled(inputs.WORKLOADS["eqb_pooled"], E=E, k=k, n_micro=3, n_tokens=16 * 37 + 5)
+    bias, mbs = inputs.router_layer(w, 300 + E, device="cuda")
+    res = _eqb_gpu(qb, mbs, bias, w.k)
+    ref = orc.eqb_global_batch([host_logits(m) for m in mbs], bias.cpu().numpy(), w.k)
+    _check_eqb(res, ref)

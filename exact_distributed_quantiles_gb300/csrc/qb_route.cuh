@@ -19,10 +19,11 @@
 //   phase A  element-wise over the tile, 8 experts per lane: s = sigma(x)
 //            (packed f32x2 arithmetic) written back in place, v = s + b, the
 //            max of every group of 8 experts;
-//   phase B  one lane per token: the (k+1)-th largest group max is a lower
-//            bound tau of alpha; only groups whose max reaches tau can hold
-//            any of the k+1 largest v, so alpha is the (k+1)-th largest v of
-//            those groups (a register insertion network);
+//   phase B  32/TILE lanes per token: the (k+1)-th largest group max is a
+//            lower bound tau of alpha; only groups whose max reaches tau can
+//            hold any of the k+1 largest v, so alpha is the (k+1)-th largest
+//            v of those groups (register sorting networks and bitonic merges,
+//            the token's lanes merging by shuffles);
 //   phase C  element-wise: r = alpha - s, packed BF16 conversion, key map,
 //            keys out, histogram increments; rows freed here are refilled at
 //            once with the warp's next tile.
@@ -93,7 +94,8 @@ struct Smem {
   static constexpr int kStatic = 256 + E * 4 + 1024;  // static lut + bias, and a margin
   static constexpr int kFixed = kHist + kStatic;
   static constexpr int kTileBytes = TILE * E * 4;  // fp32 scores; bf16 input sits in the upper half
-  static constexpr int kGmax = round16(TILE * (GE::GP > 16 ? GE::GP : 16) * 4);
+  // group maxima, later reused for the per-lane top-k lists (32 x 16 ints)
+  static constexpr int kGmax = round16(TILE * GE::GP * 4 > 2048 ? TILE * GE::GP * 4 : 2048);
   static constexpr int kAlpha = round16(TILE * 4);
   static constexpr int GR = (256 / E) > 4 ? 256 / E : 4;  // rows per load group
   static constexpr int NGRP = TILE / GR;                   // mbarriers per warp
@@ -155,12 +157,12 @@ __device__ __forceinline__ void merge_block8(float (&L)[KL], float (&v)[8]) {
   merge_desc<KL>(L, B);
 }
 
-// Merge the partner lane's list (lane ^ 16) into L.
+// Merge the list of lane ^ o into L.
 template <int KL>
-__device__ __forceinline__ void merge_partner(float (&L)[KL]) {
+__device__ __forceinline__ void merge_partner(float (&L)[KL], int o) {
   float P[KL];
 #pragma unroll
-  for (int i = 0; i < KL; ++i) P[i] = __shfl_xor_sync(0xffffffffu, L[i], 16);
+  for (int i = 0; i < KL; ++i) P[i] = __shfl_xor_sync(0xffffffffu, L[i], o);
   merge_desc<KL>(L, P);
 }
 
@@ -288,7 +290,7 @@ __device__ __forceinline__ uint32_t lut_load(const uint8_t* lut, uint32_t bin) {
 
 template <int E, int KL, int K1, typename T, int MODE, int TILE>
 __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kernel(const Args a) {
-  static_assert(TILE == 16, "phase B pairs two lanes per token of a 16-token tile");
+  static_assert(TILE == 8 || TILE == 16 || TILE == 32, "lanes per token must divide 32");
   using GE = Geo<E, TILE>;
   using SM = Smem<E, T, MODE, TILE>;
   constexpr int NW = SM::NW;
@@ -426,14 +428,16 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
     if (!__all_sync(0xffffffffu, ok)) break;
     const bool tile_ext = __any_sync(0xffffffffu, ext);
 
-    // ---- phase B: two lanes per token (lane & 15 = token, lane >> 4 = half).
-    // tau: each lane takes the top KL of its half of the group maxima, the
-    // pair merges.  alpha: the candidate groups (max >= tau) are dealt out by
-    // rank parity; each lane merges its groups' sorted values, the pair merges.
+    // ---- phase B: LPT = 32 / TILE lanes per token (lane % TILE = token,
+    // lane / TILE = part).  tau: each lane takes the top KL of its part of the
+    // group maxima, the lanes of a token merge theirs by shuffles.  alpha: the
+    // candidate groups (max >= tau) are dealt out by rank modulo LPT; each
+    // lane merges its groups' sorted values, then the token's lanes merge.
     {
-      constexpr int GH = GE::G / 2;
-      const int t = lane & 15;
-      const int h = lane >> 4;
+      constexpr int LPT = 32 / TILE;
+      constexpr int GH = GE::G / LPT;
+      const int t = lane & (TILE - 1);
+      const int h = lane / TILE;
       const bool actB = t < rows;
       float gm[GH];
       if constexpr (GH % 4 == 0) {
@@ -462,26 +466,26 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
 #pragma unroll
         for (int g = 0; g < GH; ++g) insert_desc<KL>(L, gm[g]);
       }
-      merge_partner<KL>(L);
-      const float tau = pick<KL, K1>(L, k);
-      uint32_t own = 0;
 #pragma unroll
-      for (int g = 0; g < GH; ++g) own |= (gm[g] >= tau ? 1u : 0u) << g;
-      own = actB ? own : 0u;
-      const uint32_t oth = __shfl_xor_sync(0xffffffffu, own, 16);
-      const uint64_t cand = h ? (((uint64_t)own << GH) | oth) : (((uint64_t)oth << GH) | own);
+      for (int o = TILE; o < 32; o <<= 1) merge_partner<KL>(L, o);
+      const float tau = pick<KL, K1>(L, k);
+      uint64_t cand = 0;
+#pragma unroll
+      for (int g = 0; g < GH; ++g) cand |= (gm[g] >= tau ? 1ull : 0ull) << (h * GH + g);
+      cand = actB ? cand : 0ull;
+#pragma unroll
+      for (int o = TILE; o < 32; o <<= 1) cand |= __shfl_xor_sync(0xffffffffu, cand, o);
 #pragma unroll
       for (int i = 0; i < KL; ++i) L[i] = -INFINITY;
       const float* srow = sc + t * E;
       for (uint64_t m = cand; m;) {
-        const int g0 = __ffsll((long long)m) - 1;
-        m &= m - 1;
-        int g1 = -1;
-        if (m) {
-          g1 = __ffsll((long long)m) - 1;
+        int g = -1;
+#pragma unroll
+        for (int p = 0; p < LPT; ++p) {
+          const int gp = m ? __ffsll((long long)m) - 1 : -1;
           m &= m - 1;
+          g = (p == h) ? gp : g;
         }
-        const int g = h ? g1 : g0;
         if (g >= 0) {
           float s8[8], b8[8];
           load8(srow + 8 * g, s8);
@@ -493,7 +497,8 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
           merge_block8<KL>(L, s8);
         }
       }
-      merge_partner<KL>(L);
+#pragma unroll
+      for (int o = TILE; o < 32; o <<= 1) merge_partner<KL>(L, o);
       const float alpha = pick<KL, K1>(L, k);
       const int64_t tok = t0 + t;
       if (actB && h == 0) {
@@ -527,37 +532,44 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
             }
           }
         } else {
-          // the k experts above alpha: each lane writes its own from one end
-          // of the token's list in shared memory, then one lane sorts them
-          int32_t* lst = reinterpret_cast<int32_t*>(gmax) + t * 16;
+          // the k experts above alpha: each lane lists its own in a 16-slot
+          // shared list (slot 15 = count), one lane per token merges and sorts
+          int32_t* lst = reinterpret_cast<int32_t*>(gmax) + (t * LPT + h) * 16;
           int c = 0;
           for (uint64_t m = cand; m;) {
-            const int g0 = __ffsll((long long)m) - 1;
-            m &= m - 1;
-            int g1 = -1;
-            if (m) {
-              g1 = __ffsll((long long)m) - 1;
+            int g = -1;
+#pragma unroll
+            for (int p = 0; p < LPT; ++p) {
+              const int gp = m ? __ffsll((long long)m) - 1 : -1;
               m &= m - 1;
+              g = (p == h) ? gp : g;
             }
-            const int g = h ? g1 : g0;
             if (g >= 0) {
               float s8[8], b8[8];
               load8(srow + 8 * g, s8);
               load8(bias_s + 8 * g, b8);
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                if (__fadd_rn(s8[i], b8[i]) > alpha) {
-                  lst[h ? k - 1 - c : c] = 8 * g + i;
-                  ++c;
-                }
-              }
+              for (int i = 0; i < 8; ++i)
+                if (__fadd_rn(s8[i], b8[i]) > alpha && c < 15) lst[c++] = 8 * g + i;
             }
           }
+          lst[15] = c;
           __syncwarp();
           if (actB && h == 0) {
             int v[KL];
+            int n = 0;
 #pragma unroll
-            for (int i = 0; i < KL; ++i) v[i] = i < k ? lst[i] : INT_MAX;
+            for (int i = 0; i < KL; ++i) v[i] = INT_MAX;
+            for (int p = 0; p < LPT; ++p) {
+              const int32_t* lp = reinterpret_cast<int32_t*>(gmax) + (t * LPT + p) * 16;
+              const int cp = lp[15];
+              for (int i = 0; i < cp; ++i) {
+                const int idx = lp[i];
+#pragma unroll
+                for (int q = 0; q < KL; ++q) v[q] = (q == n) ? idx : v[q];
+                ++n;
+              }
+            }
 #pragma unroll
             for (int i = 0; i < KL; ++i)
 #pragma unroll
@@ -714,7 +726,7 @@ int dispatch_E(int E, int k, const Args& a, cudaStream_t st) {
 }
 
 #ifndef QB_ROUTE_TILE
-#define QB_ROUTE_TILE 16
+#define QB_ROUTE_TILE 8
 #endif
 
 template <int MODE>

@@ -37,8 +37,27 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 METRIC = "QB routed tokens/s per layer (E=256,k=6, 2-pass EQB) on 1 GB300; % of HBM roofline"
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one route-kernel
+# launch on a 524288-token layer, from the ncu capture summarised in
+# profiles/route_kernel_hi_one_layer.md.  Reported only while the kernel's
+# sources hash to the value they had when the counters were taken.
+ROUTE_TRAFFIC = {"sha1": "d6b68d39288317f0c2cc0d4864ab2280de085c23", "tokens": 524288,
+                 "bytes": (537.132032 + 246.898944) * 1e6}
+ROUTE_SOURCES = ("qb_route.cuh", "qb_device.cuh", "qb_route_hi.cu")
 UNIT = "tokens/s/layer"
 WORKLOAD = "full_step"
+
+
+def _route_traffic(tokens: int):
+    import hashlib
+    h = hashlib.sha1()
+    for f in ROUTE_SOURCES:
+        with open(os.path.join(ROOT, "exact_distributed_quantiles_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest() != ROUTE_TRAFFIC["sha1"]:
+        return None
+    return ROUTE_TRAFFIC["bytes"] * tokens / ROUTE_TRAFFIC["tokens"]
 
 
 def _peaks():
@@ -236,12 +255,12 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=48)
     ap.add_argument("--ref-tokens", type=int, default=32768)
-    ap.add_argument("--cpu-tokens", type=int, default=65536)
+    ap.add_argument("--cpu-tokens", type=int, default=524288)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
@@ -330,7 +349,7 @@ def main():
             "eqb_only": {"value": eqb_value, "unit": UNIT, "ms_per_step": ms_eqb / args.steps},
             "roofline": {"bound": "hbm", "kernel": "qb_route_hist_hi (route_kernel hi mode)",
                          "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
-                         "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                         "unit": "GB/s", "frac": achieved / peak, "traffic": _route_traffic(n),
                          "bytes_per_launch": hi_bytes, "avg_launch_ms": hi_avg_ms},
             "cpu_baseline": cpu,
             "e2e": e2e,

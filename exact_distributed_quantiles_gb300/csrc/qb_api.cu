@@ -195,6 +195,27 @@ int lei_inject(float* grad, const int32_t* topk_idx, int64_t N, int E, int k, fl
   return launch_lei(grad, topk_idx, N, E, k, eta, batch_tokens, workspace, as_stream(stream));
 }
 
+int qb_router_gemm(const void* hidden, const void* w_t, int64_t M, int H, int E, float* logits_out,
+                   void* stream) {
+  if (!hidden || !w_t || !logits_out) return QB_EINVAL;
+  if (!aligned16(hidden) || !aligned16(w_t) || !aligned16(logits_out)) return QB_EINVAL;
+  if (M < 0) return QB_EINVAL;
+  if (M > INT32_MAX) return QB_EOVERFLOW;
+  if (E != 256 || H < 64 || H % 64 != 0) return QB_EUNSUPPORTED;
+  if (M == 0) return QB_OK;
+  return launch_router_gemm(hidden, w_t, M, H, E, logits_out, as_stream(stream));
+}
+
+int qb_router_gemm_hist_hi(const void* hidden, const void* w_t, int64_t M, int H, int E, int k,
+                           const float* bias, float* logits_out, int32_t* hist_hi,
+                           uint16_t* keys_out, int32_t* topk_out, float* alpha_out,
+                           void* stream) {
+  int st = qb_router_gemm(hidden, w_t, M, H, E, logits_out, stream);
+  if (st != QB_OK || M == 0) return st;
+  return qb_route_hist_hi(logits_out, QB_F32, bias, M, E, k, hist_hi, keys_out, topk_out,
+                          alpha_out, stream);
+}
+
 int qb_device_status(int* flags_out) {
   int* p = device_status_ptr();
   if (!p) return QB_ECUDA;

@@ -22,7 +22,7 @@ QB_F32, QB_BF16 = 0, 1
 EXPORTS = ("qb_status_string", "qb_version", "qb_rank", "qb_sigmoid", "qb_zero_i32",
            "qb_route_hist_hi", "qb_select_hi", "qb_keys_hist_lo", "qb_route_hist_lo",
            "qb_finalize", "k3_route_hist", "k3_finalize", "lei_inject", "qb_device_status",
-           "lei_inject_noalloc")
+           "lei_inject_noalloc", "qb_router_gemm", "qb_router_gemm_hist_hi")
 
 
 class QBError(RuntimeError):
@@ -53,6 +53,8 @@ def _load():
         "lei_inject": (I, [P, P, I64, I, I, F, I64, P, P]),
         "qb_device_status": (I, [ctypes.POINTER(ctypes.c_int)]),
         "lei_inject_noalloc": (I, [P, P, I64, I, I, F, I64, P]),
+        "qb_router_gemm": (I, [P, P, I64, I, I, P, P]),
+        "qb_router_gemm_hist_hi": (I, [P, P, I64, I, I, I, P, P, P, P, P, P, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -181,6 +183,23 @@ def lei_inject_noalloc(grad, topk_idx, eta, batch_tokens=0, stream=None):
     _check("lei_inject_noalloc",
            lib.lei_inject_noalloc(_ptr(grad), _ptr(topk_idx), N, E, int(k), float(eta),
                                   int(batch_tokens), _stream(stream)))
+
+
+def qb_router_gemm(hidden, w_t, logits_out, stream=None):
+    M, H = hidden.shape
+    E = w_t.shape[0]
+    _check("qb_router_gemm", lib.qb_router_gemm(_ptr(hidden), _ptr(w_t), M, H, E, _ptr(logits_out),
+                                                _stream(stream)))
+
+
+def qb_router_gemm_hist_hi(hidden, w_t, bias, k, logits_out, hist_hi, keys_out=None,
+                           topk_out=None, alpha_out=None, stream=None):
+    M, H = hidden.shape
+    E = w_t.shape[0]
+    _check("qb_router_gemm_hist_hi",
+           lib.qb_router_gemm_hist_hi(_ptr(hidden), _ptr(w_t), M, H, E, int(k), _ptr(bias),
+                                      _ptr(logits_out), _ptr(hist_hi), _ptr(keys_out),
+                                      _ptr(topk_out), _ptr(alpha_out), _stream(stream)))
 
 
 def device_status() -> int:

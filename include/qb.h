@@ -176,6 +176,29 @@ int k3_finalize(int32_t* hist, int E, int nbins, int64_t r, float* bounds, float
 int lei_inject(float* grad, const int32_t* topk_idx, int64_t N, int E, int k, float eta,
                int64_t batch_tokens, float* workspace, void* stream);
 
+/* --------------------------------------------------------- router GEMM ---- */
+
+/* Router logits on the tensor cores: logits[M, E] = hidden[M, H] x W[H, E],
+ * bf16 inputs, fp32 accumulation (tcgen05.mma, accumulator in tensor memory).
+ * The router of [QB-PR] ("Implementation": the histogram is added to the
+ * existing router kernel) produces these scores.
+ *   hidden     device bf16 [M, H] row-major, 16-byte aligned.
+ *   w_t        device bf16 [E, H]: W transposed (each expert's column of W
+ *              contiguous), 16-byte aligned.
+ *   logits_out device fp32 [M, E], 16-byte aligned.
+ * Supported: E = 256, H a positive multiple of 64.  The accumulation order
+ * over H is the tensor core's; results agree with an fp64 product within
+ * fp32 accumulation error. */
+int qb_router_gemm(const void* hidden, const void* w_t, int64_t M, int H, int E, float* logits_out,
+                   void* stream);
+
+/* Router GEMM followed by the EQB hi pass on its logits (same outputs as
+ * qb_route_hist_hi on logits_out, which is required: the hi pass reads it). */
+int qb_router_gemm_hist_hi(const void* hidden, const void* w_t, int64_t M, int H, int E, int k,
+                           const float* bias, float* logits_out, int32_t* hist_hi,
+                           uint16_t* keys_out, int32_t* topk_out, float* alpha_out,
+                           void* stream);
+
 /* Load-error injection without a caller workspace.  The pages have no
  * counterpart to this entry point; it exists for callers that cannot allocate
  * device memory where LEI is applied -- code under a framework whose caching

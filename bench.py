@@ -64,9 +64,9 @@ def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         d = json.load(open(p))
-        return float(d["hbm_gbs"]), "measured"
+        return float(d["hbm_gbs"]), "measured", d
     except Exception:
-        return 6800.0, "fallback"
+        return 6800.0, "fallback", {"bf16_tflops": 1900.0}
 
 
 class ClockSampler:
@@ -198,6 +198,110 @@ def _timed(fn, steps, warmup, dist_on):
     return ms
 
 
+def _per_call_ms(fn, reps, warmup):
+    """Mean device time of one fn() over reps back-to-back calls (CUDA events)."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def components(qb, inputs, dev, reps, warmup, peak_hbm, peaks):
+    """The other two timed paths: K3 histogram mode and the router-GEMM front end.
+
+    K3: E=256, k=8, 4 x 65536 bf16 tokens, 1000 bins; one global batch = four
+    k3_route_hist calls + k3_finalize.  Four copies of the batch at distinct
+    addresses (512 MiB together) are used in turn so that L2 holds none of
+    them.  Router GEMM: 4 x 32768 tokens of bf16 hidden states [., 2048] x W
+    [2048, 256]; one global batch = four GEMM + hi-pass calls, select, lo pass
+    over the stored keys, finalize.  Its 512 MiB of hidden states exceed L2."""
+    out = {}
+    # ---- K3
+    w3 = inputs.WORKLOADS["k3"]
+    bias3, mbs3 = inputs.router_layer(w3, inputs.seed_for("k3"), device=dev)
+    copies = [[m.clone() for m in mbs3] for _ in range(4)]
+    bounds = inputs.k3_initial_bounds(bias3).to(dev)
+    hist3 = torch.zeros(w3.E, 1000, dtype=torch.int32, device=dev)
+    ws3 = torch.empty(w3.n_tokens, w3.E, dtype=torch.int16, device=dev)
+    b3 = bias3.clone()
+    R3 = qb.rank(w3.n_pool, w3.E, w3.k)
+    it = [0]
+
+    def k3_hist_only():
+        for m in copies[it[0] % 4]:
+            qb.k3_route_hist(m, b3, w3.k, bounds, hist3, ws3)
+        it[0] += 1
+
+    def k3_batch():
+        k3_hist_only()
+        qb.k3_finalize(hist3, R3, bounds, b3, reset=True)
+
+    ms_batch = _per_call_ms(k3_batch, reps, warmup)
+    ms_hist = _per_call_ms(k3_hist_only, reps, warmup)
+    qb.qb_zero_i32(hist3)
+    k3_bytes = w3.n_pool * w3.E * 2  # bf16 logits read once (algorithmic)
+    out["k3"] = {
+        "workload": "k3: 4x65536 bf16 tokens, E=256, k=8, 1000 bins",
+        "value": w3.n_pool / (ms_batch / 1e3), "unit": "tokens/s", "ms_per_batch": ms_batch,
+        "launches_per_batch": 2 * w3.n_micro + 1,
+        "roofline": {"bound": "hbm", "kernel": "k3_route_hist (route_kernel K3 mode + k3_count)",
+                     "achieved": k3_bytes / (ms_hist / 1e3) / 1e9, "peak": peak_hbm,
+                     "unit": "GB/s", "frac": k3_bytes / (ms_hist / 1e3) / 1e9 / peak_hbm,
+                     "bytes_per_batch": k3_bytes, "hist_ms_per_batch": ms_hist}}
+    del copies, mbs3
+
+    # ---- router GEMM front end
+    w5 = inputs.WORKLOADS["router_gemm"]
+    bias5, W, hs = inputs.gemm_layer(w5, inputs.seed_for("router_gemm"), device=dev)
+    w_t = W.t().contiguous()
+    n, E, H = w5.n_tokens, w5.E, w5.hidden
+    logits5 = torch.empty(n, E, dtype=torch.float32, device=dev)
+    keys5 = torch.empty(w5.n_pool, E, dtype=torch.int16, device=dev)
+    hi5 = torch.zeros(E, 256, dtype=torch.int32, device=dev)
+    lo5 = torch.zeros(E, 256, dtype=torch.int32, device=dev)
+    sel5 = torch.zeros(E, dtype=torch.int32, device=dev)
+    rlo5 = torch.zeros(E, dtype=torch.int32, device=dev)
+    b5 = bias5.clone()
+    R5 = qb.rank(w5.n_pool, E, w5.k)
+
+    def gemm_only():
+        for h in hs:
+            qb.qb_router_gemm(h, w_t, logits5)
+
+    def gemm_batch():
+        for i, h in enumerate(hs):
+            qb.qb_router_gemm_hist_hi(h, w_t, b5, w5.k, logits5, hi5,
+                                      keys_out=keys5[i * n:(i + 1) * n])
+        qb.qb_select_hi(hi5, R5, sel5, rlo5)
+        qb.qb_keys_hist_lo(keys5, sel5, lo5)
+        qb.qb_finalize(hi5, lo5, sel5, rlo5, b5, reset=True)
+
+    ms5 = _per_call_ms(gemm_batch, reps, warmup)
+    ms_g = _per_call_ms(gemm_only, reps, warmup)
+    flops = 2.0 * w5.n_pool * H * E
+    gbytes = w5.n_pool * H * 2 + H * E * 2 * w5.n_micro + w5.n_pool * E * 4
+    tflops = flops / (ms_g / 1e3) / 1e12
+    out["router_gemm"] = {
+        "workload": "router_gemm: 4x32768 tokens, hidden 2048 bf16 x W [2048,256] bf16 -> fp32 "
+                    "logits, then EQB (k=6) on them",
+        "value": w5.n_pool / (ms5 / 1e3), "unit": "tokens/s", "ms_per_batch": ms5,
+        "launches_per_batch": 2 * w5.n_micro + 3,
+        "roofline": {"bound": "tensor", "kernel": "router_gemm_kernel (tcgen05, TMEM)",
+                     "achieved": tflops, "peak": peaks.get("bf16_tflops"), "unit": "TFLOP/s",
+                     "frac": tflops / peaks["bf16_tflops"] if peaks.get("bf16_tflops") else None,
+                     "gemm_ms_per_batch": ms_g,
+                     "hbm_gbs": gbytes / (ms_g / 1e3) / 1e9, "hbm_frac": gbytes / (ms_g / 1e3)
+                     / 1e9 / peak_hbm}}
+    return out
+
+
 def cpu_baseline_sample(n_tokens: int, layer: int = 0):
     """Oracle on a bounded sample: n_tokens of one full-step layer through EQB
     (route by full sort, keys, hi/lo counts, exact select by sort, centering)
@@ -263,6 +367,7 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=524288)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-components", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -296,7 +401,7 @@ def main():
     value = world * tokens_layer_step / (ms_step / 1e3)
     eqb_value = world * tokens_layer_step / ((ms_eqb / args.steps) / 1e3)
 
-    peak, peak_kind = _peaks()
+    peak, peak_kind, peaks = _peaks()
     n, E, k = w.n_pool, w.E, w.k
     hi_bytes = n * E * (4 + 2) + n * k * 4   # logits read, keys write, top-k write
     hi_avg_ms = statistics.mean(hi_ms) if hi_ms else float("nan")
@@ -326,6 +431,11 @@ def main():
                "h2d_bytes_per_step": fs.L * 2 * n * E * 4,
                "d2h_bytes_per_step": fs.L * (n * E * 4 + E * 4), "steps": e2e_steps}
 
+    comps = None
+    if not args.no_components:
+        comps = components(qb, inputs, fs.logits.device, max(args.steps, 10), args.warmup, peak,
+                           peaks)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         dt, nt, cores = cpu_baseline_sample(args.cpu_tokens)
@@ -353,6 +463,7 @@ def main():
                          "bytes_per_launch": hi_bytes, "avg_launch_ms": hi_avg_ms},
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "components": comps,
             "gpu_launches": args.steps * fs.L * (fs.launches_per_layer["eqb"]
                                                  + fs.launches_per_layer["lei"]),
             "clocks": clk.summary(),

@@ -160,14 +160,19 @@ int qb_finalize(int32_t* hist_hi, int32_t* hist_lo, const int32_t* sel, const in
 }
 
 int k3_route_hist(const void* logits, int dtype, const float* bias, int64_t N, int E, int k,
-                  const float* bounds, int nbins, int32_t* hist, void* stream) {
+                  const float* bounds, int nbins, int32_t* hist, uint16_t* bins_ws,
+                  void* stream) {
   int st = check_route_args(logits, dtype, bias, N, E, k);
   if (st != QB_OK) return st;
-  if (!bounds || !hist) return QB_EINVAL;
+  if (!bounds || !hist || !bins_ws) return QB_EINVAL;
+  if (!aligned16(bins_ws)) return QB_EINVAL;
   if (nbins < 1 || nbins > 65536) return QB_EINVAL;
   if (N == 0) return QB_OK;
-  return launch_route_k3(logits, dtype, bias, N, E, k, hist, nullptr, nullptr, nullptr, nullptr,
-                         bounds, nbins, as_stream(stream));
+  cudaStream_t s = as_stream(stream);
+  st = launch_route_k3(logits, dtype, bias, N, E, k, nullptr, bins_ws, nullptr, nullptr, nullptr,
+                       bounds, nbins, s);
+  if (st != QB_OK) return st;
+  return launch_k3_count(bins_ws, N, E, nbins, hist, s);
 }
 
 int k3_finalize(int32_t* hist, int E, int nbins, int64_t r, float* bounds, float* bias_out,

@@ -256,91 +256,6 @@ __global__ void __launch_bounds__(512) eqb_center_kernel(float* __restrict__ bia
     bias_out[j] = __double2float_rn(__dsub_rn((double)q_s[j], mu));
 }
 
-// First index where the inclusive prefix sum of the row reaches `target`, or
-// -1; `before` receives the sum of the bins below it.  One warp.
-__device__ int warp_first_reaching(const int32_t* __restrict__ row, int nbins, long long target,
-                                   long long* before_out) {
-  const int lane = threadIdx.x & 31;
-  long long base = 0;
-  for (int c0 = 0; c0 < nbins; c0 += 32) {
-    const int b = c0 + lane;
-    const long long c = (b < nbins) ? row[b] : 0;
-    long long v = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long y = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += y;
-    }
-    const long long cum = base + v;
-    const unsigned hit = __ballot_sync(0xffffffffu, b < nbins && cum >= target);
-    if (hit) {
-      const int src = __ffs(hit) - 1;
-      const long long cum_at = __shfl_sync(0xffffffffu, cum, src);
-      const long long c_at = __shfl_sync(0xffffffffu, c, src);
-      *before_out = cum_at - c_at;
-      return c0 + src;
-    }
-    base = __shfl_sync(0xffffffffu, cum, 31);
-  }
-  *before_out = base;
-  return -1;
-}
-
-// ------------------------------------------------------------------------
-// K3 finalize: one CTA of 1024 threads, warp per expert for the bin search,
-// then serial fp64 centering and the new bounds.
-// ------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) k3_finalize_kernel(const int32_t* __restrict__ hist, int E,
-                                                          int nbins, long long r,
-                                                          float* __restrict__ bounds,
-                                                          float* __restrict__ bias_out) {
-  __shared__ double q_s[512];
-  __shared__ double mu_s;
-  __shared__ float lo_s, hi_s;
-  if (threadIdx.x == 0) {
-    lo_s = bounds[0];
-    hi_s = bounds[1];
-  }
-  __syncthreads();
-  const double dlo = (double)lo_s;
-  const double width = __ddiv_rn(__dsub_rn((double)hi_s, dlo), (double)nbins);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int j = warp; j < E; j += 32) {
-    long long before = 0;
-    const int32_t* row = hist + (int64_t)j * nbins;
-    const int b = warp_first_reaching(row, nbins, r, &before);
-    if (lane == 0) {
-      if (b < 0) {
-        q_s[j] = (double)hi_s;
-      } else {
-        const double edge = __dadd_rn(dlo, __dmul_rn((double)b, width));
-        const double frac = __ddiv_rn((double)(r - before), (double)row[b]);
-        q_s[j] = __dadd_rn(edge, __dmul_rn(width, frac));
-      }
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double sum = 0.0;
-    for (int j = 0; j < E; ++j) sum = __dadd_rn(sum, q_s[j]);
-    mu_s = __ddiv_rn(sum, (double)E);
-  }
-  __syncthreads();
-  for (int j = threadIdx.x; j < E; j += blockDim.x)
-    bias_out[j] = __double2float_rn(__dsub_rn(q_s[j], mu_s));
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float mn = bias_out[0], mx = bias_out[0];
-    for (int j = 1; j < E; ++j) {
-      const float v = bias_out[j];
-      mn = v < mn ? v : mn;
-      mx = v > mx ? v : mx;
-    }
-    bounds[0] = __fsub_rn(mn, 1.0f);
-    bounds[1] = __fadd_rn(mx, 1.0f);
-  }
-}
-
 // ------------------------------------------------------------------------
 // Utilities.
 // ------------------------------------------------------------------------
@@ -418,14 +333,6 @@ int launch_finalize(int32_t* hist_hi, int32_t* hist_lo, const int32_t* sel, cons
   if (st != QB_OK) return st;
   eqb_center_kernel<<<1, 512, 0, stream>>>(bias_out, E);
   return launch_status();
-}
-
-int launch_k3_finalize(int32_t* hist, int E, int nbins, int64_t r, float* bounds,
-                       float* bias_out, int reset, cudaStream_t stream) {
-  k3_finalize_kernel<<<1, 1024, 0, stream>>>(hist, E, nbins, (long long)r, bounds, bias_out);
-  int st = launch_status();
-  if (st != QB_OK || !reset) return st;
-  return launch_zero_i32(hist, (int64_t)E * nbins, stream);
 }
 
 int launch_sigmoid(const float* x, float* s, int64_t n, cudaStream_t stream) {

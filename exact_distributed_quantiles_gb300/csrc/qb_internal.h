@@ -42,6 +42,8 @@ int launch_finalize(int32_t* hist_hi, int32_t* hist_lo, const int32_t* sel, cons
                     int E, float* bias_out, uint16_t* qkey_out, int reset, cudaStream_t stream);
 int launch_k3_finalize(int32_t* hist, int E, int nbins, int64_t r, float* bounds,
                        float* bias_out, int reset, cudaStream_t stream);
+int launch_k3_count(const uint16_t* bins, int64_t N, int E, int nbins, int32_t* hist,
+                    cudaStream_t stream);
 int launch_zero_i32(int32_t* p, int64_t n, cudaStream_t stream);
 int launch_sigmoid(const float* x, float* s, int64_t n, cudaStream_t stream);
 int launch_lei(float* grad, const int32_t* topk, int64_t N, int E, int k, float eta,

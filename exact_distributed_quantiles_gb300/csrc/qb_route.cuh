@@ -51,8 +51,8 @@ struct Args {
   const float* bias;
   int64_t N;
   int k;
-  int32_t* hist;  // hi: [E,256]  lo: [E,256]  k3: [E,nbins]
-  uint16_t* keys_out;
+  int32_t* hist;  // hi: [E,256]  lo: [E,256]  k3: unused
+  uint16_t* keys_out;  // hi: EQB keys [N,E] (optional)  k3: bin indices [N,E]
   int32_t* topk_out;
   float* alpha_out;
   const int32_t* sel;   // lo mode
@@ -601,19 +601,21 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
           float s[8];
           load8(sc + f, s);
           const float alpha = alpha_s[row];
+          uint32_t bw[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float r = __fsub_rn(alpha, s[i]);
             const float tt = __fmul_rn(__fsub_rn(r, k3_lo), k3_scale);
-            int idx;
+            uint32_t idx;
             if (!(tt >= 0.0f))
-              idx = 0;
+              idx = 0u;
             else if (tt >= k3_nb)
-              idx = a.nbins - 1;
+              idx = (uint32_t)(a.nbins - 1);
             else
-              idx = __float2int_rz(tt);
-            atomicAdd(a.hist + (int64_t)(e0 + i) * a.nbins + idx, 1);
+              idx = (uint32_t)__float2int_rz(tt);
+            bw[i >> 1] |= idx << ((i & 1) * 16);
           }
+          *reinterpret_cast<uint4*>(a.keys_out + tok * E + e0) = make_uint4(bw[0], bw[1], bw[2], bw[3]);
         }
       } else {
         uint32_t kw[4] = {0u, 0u, 0u, 0u};

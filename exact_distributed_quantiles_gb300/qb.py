@@ -48,7 +48,7 @@ def _load():
         "qb_keys_hist_lo": (I, [P, I64, I, P, P, P]),
         "qb_route_hist_lo": (I, [P, I, P, I64, I, I, P, P, P]),
         "qb_finalize": (I, [P, P, P, P, I, P, P, I, P]),
-        "k3_route_hist": (I, [P, I, P, I64, I, I, P, I, P, P]),
+        "k3_route_hist": (I, [P, I, P, I64, I, I, P, I, P, P, P]),
         "k3_finalize": (I, [P, I, I, I64, P, P, I, P]),
         "lei_inject": (I, [P, P, I64, I, I, F, I64, P, P]),
         "qb_device_status": (I, [ctypes.POINTER(ctypes.c_int)]),
@@ -153,12 +153,12 @@ def qb_finalize(hist_hi, hist_lo, sel, r_lo, bias_out, qkey_out=None, reset=True
                            _ptr(qkey_out), 1 if reset else 0, _stream(stream)))
 
 
-def k3_route_hist(logits, bias, k, bounds, hist, stream=None):
+def k3_route_hist(logits, bias, k, bounds, hist, bins_ws, stream=None):
     N, E = logits.shape
     nbins = hist.shape[1]
     _check("k3_route_hist",
            lib.k3_route_hist(_ptr(logits), _dtype(logits), _ptr(bias), N, E, int(k), _ptr(bounds),
-                             nbins, _ptr(hist), _stream(stream)))
+                             nbins, _ptr(hist), _ptr(bins_ws), _stream(stream)))
 
 
 def k3_finalize(hist, r, bounds, bias_out, reset=True, stream=None):

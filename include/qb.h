@@ -145,10 +145,17 @@ int qb_finalize(int32_t* hist_hi, int32_t* hist_lo, const int32_t* sel, const in
  *   w = RN(hi - lo), scale = RN(nbins / w),
  *   idx = floor(RN(RN(r - lo) * scale)), clamped to [0, nbins-1],
  *   hist[j][idx] += 1, with r the fp32 margin.
- *   bounds device fp32 [2] = {lo, hi}, lo < hi (read on the device).
- *   hist   device int32 [E, nbins]; 1 <= nbins <= 65536. */
+ *   bounds  device fp32 [2] = {lo, hi}, lo < hi (read on the device).
+ *   hist    device int32 [E, nbins]; 1 <= nbins <= 65536.
+ *   bins_ws device uint16 [N, E] scratch owned by the caller, 16-byte
+ *           aligned: the routing pass stores every idx there and a second
+ *           kernel counts them (the histogram is too large to privatise per
+ *           CTA whole).  Its contents afterwards are the bin indices.
+ * Two launches on `stream`; the workspace must not be shared by calls that
+ * may run concurrently. */
 int k3_route_hist(const void* logits, int dtype, const float* bias, int64_t N, int E, int k,
-                  const float* bounds, int nbins, int32_t* hist, void* stream);
+                  const float* bounds, int nbins, int32_t* hist, uint16_t* bins_ws,
+                  void* stream);
 
 /* K3 quantile, centering and next bounds ([QB-PR] "Quantile estimator"):
  *   b*  = first bin with cumulative count >= r, before = count below it,
@@ -156,6 +163,10 @@ int k3_route_hist(const void* logits, int dtype, const float* bias, int64_t N, i
  *         width = (hi - lo) / nbins;
  *   bias_out[j] = RN32(q_j - mean_j q_j);
  *   bounds <- {min_j bias_out - 1, max_j bias_out + 1} (fp32, in place).
+ * The fp64 sum behind the mean is a fixed tree (per-CTA halves of 8 groups
+ * of E/8 experts, then the 8 partial sums in order), not the ascending
+ * serial order: the result agrees with the serial sum to well within the
+ * 1e-6 relative tolerance of this mode.  E must be a multiple of 8, E <= 512.
  * reset != 0 zeroes hist afterwards.  bounds and bias_out are device. */
 int k3_finalize(int32_t* hist, int E, int nbins, int64_t r, float* bounds, float* bias_out,
                 int reset, void* stream);

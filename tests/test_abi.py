@@ -92,8 +92,10 @@ def test_argument_errors_are_reported_before_launch(lib):
     assert L.qb_finalize(fake, fake, fake, fake, 256, N0, N0, 1, N0) == lib.QB_EINVAL
     assert L.qb_finalize(N0, fake, fake, fake, 256, fake, N0, 1, N0) == lib.QB_EINVAL
     # K3
-    assert L.k3_route_hist(fake, 1, fake, 10, 256, 8, fake, 0, fake, N0) == lib.QB_EINVAL
-    assert L.k3_route_hist(fake, 1, fake, 10, 256, 8, N0, 1000, fake, N0) == lib.QB_EINVAL
+    assert L.k3_route_hist(fake, 1, fake, 10, 256, 8, fake, 0, fake, fake, N0) == lib.QB_EINVAL
+    assert L.k3_route_hist(fake, 1, fake, 10, 256, 8, N0, 1000, fake, fake, N0) == lib.QB_EINVAL
+    assert L.k3_route_hist(fake, 1, fake, 10, 256, 8, fake, 1000, fake, N0, N0) == lib.QB_EINVAL
+    assert L.k3_route_hist(fake, 1, fake, 10, 256, 8, fake, 1000, fake, odd, N0) == lib.QB_EINVAL
     assert L.k3_finalize(fake, 256, 1000, 0, fake, fake, 1, N0) == lib.QB_EINVAL
     assert L.k3_finalize(fake, 256, 70000, 5, fake, fake, 1, N0) == lib.QB_EINVAL
     # LEI

@@ -2,7 +2,8 @@
 
 K3: "[Dev] Add global-batch quantile balancing", "Quantile estimator" and
 "Implementation" -- counts exact, biases within 1e-6 relative to the bias
-vector's scale (bit equality expected: both sides run the same fp64 steps).
+vector's scale (the GPU sums the fp64 quantiles in a fixed tree, the oracle
+in ascending order; everything before that is the same fp64 steps).
 LEI: "Exact Quantile Balancing and Load-Error Injection for Mixture-of-
 Experts", LEI paragraph -- gradients within 1e-6 absolute.
 Sigmoid: the score function, bit-equal to the oracle over all 2^32 inputs.
@@ -57,8 +58,9 @@ def _k3_gpu(qb, mbs, bias, k, bounds0, nbins):
     E = bias.shape[0]
     hist = torch.zeros(E, nbins, dtype=torch.int32, device="cuda")
     bounds = bounds0.clone().cuda()
+    ws = torch.empty(max(m.shape[0] for m in mbs), E, dtype=torch.int16, device="cuda")
     for m in mbs:
-        qb.k3_route_hist(m, bias, k, bounds, hist)
+        qb.k3_route_hist(m, bias, k, bounds, hist, ws[:m.shape[0]])
     n_pool = sum(m.shape[0] for m in mbs)
     h = hist.clone()
     b_out = torch.empty_like(bias)

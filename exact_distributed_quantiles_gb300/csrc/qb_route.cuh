@@ -36,6 +36,8 @@
 #pragma once
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "qb_device.cuh"
 #include "qb_internal.h"
 
@@ -86,6 +88,14 @@ struct Geo {
 };
 
 __host__ __device__ constexpr int round16(int b) { return (b + 15) & ~15; }
+
+// Bit mask over the groups of 8 experts of a token (32 bits up to E = 256).
+template <int G>
+using GroupMask = typename std::conditional<(G <= 32), uint32_t, unsigned long long>::type;
+__device__ __forceinline__ int lowest_bit(uint32_t m) { return __ffs((int)m) - 1; }  // -1 if 0
+__device__ __forceinline__ int lowest_bit(unsigned long long m) {
+  return __ffsll((long long)m) - 1;
+}
 
 template <int E, typename T, int MODE, int TILE>
 struct Smem {
@@ -469,20 +479,21 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
 #pragma unroll
       for (int o = TILE; o < 32; o <<= 1) merge_partner<KL>(L, o);
       const float tau = pick<KL, K1>(L, k);
-      uint64_t cand = 0;
+      using MaskT = GroupMask<GE::G>;
+      MaskT cand = 0;
 #pragma unroll
-      for (int g = 0; g < GH; ++g) cand |= (gm[g] >= tau ? 1ull : 0ull) << (h * GH + g);
-      cand = actB ? cand : 0ull;
+      for (int g = 0; g < GH; ++g) cand |= (MaskT)(gm[g] >= tau ? 1u : 0u) << (h * GH + g);
+      cand = actB ? cand : (MaskT)0;
 #pragma unroll
       for (int o = TILE; o < 32; o <<= 1) cand |= __shfl_xor_sync(0xffffffffu, cand, o);
 #pragma unroll
       for (int i = 0; i < KL; ++i) L[i] = -INFINITY;
       const float* srow = sc + t * E;
-      for (uint64_t m = cand; m;) {
+      for (MaskT m = cand; m;) {
         int g = -1;
 #pragma unroll
         for (int p = 0; p < LPT; ++p) {
-          const int gp = m ? __ffsll((long long)m) - 1 : -1;
+          const int gp = lowest_bit(m);
           m &= m - 1;
           g = (p == h) ? gp : g;
         }
@@ -516,8 +527,8 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
           // rare: a tie at alpha; one lane per token scans in index order
           if (actB && h == 0) {
             int tl = ties, c = 0;
-            for (uint64_t m = cand; m; m &= m - 1) {
-              const int g = __ffsll((long long)m) - 1;
+            for (MaskT m = cand; m; m &= m - 1) {
+              const int g = lowest_bit(m);
               float s8[8], b8[8];
               load8(srow + 8 * g, s8);
               load8(bias_s + 8 * g, b8);
@@ -532,55 +543,53 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
             }
           }
         } else {
-          // the k experts above alpha: each lane lists its own in a 16-slot
-          // shared list (slot 15 = count), one lane per token merges and sorts
-          int32_t* lst = reinterpret_cast<int32_t*>(gmax) + (t * LPT + h) * 16;
-          int c = 0;
-          for (uint64_t m = cand; m;) {
-            int g = -1;
+          // The k experts above alpha in ascending order.  Only groups whose
+          // max exceeds alpha hold any; the token's lanes take each of them
+          // in turn, lane h testing EPL consecutive elements, and EPL warp
+          // ballots tell every lane how many of the group's elements below
+          // its own are set, so each index goes straight to its slot.
+          constexpr int EPL = 8 / LPT;
+          constexpr uint32_t PAT = TILE == 8 ? 0x01010101u : (TILE == 16 ? 0x00010001u : 1u);
+          MaskT gsel = 0;
 #pragma unroll
-            for (int p = 0; p < LPT; ++p) {
-              const int gp = m ? __ffsll((long long)m) - 1 : -1;
-              m &= m - 1;
-              g = (p == h) ? gp : g;
+          for (int g = 0; g < GH; ++g) gsel |= (MaskT)(gm[g] > alpha ? 1u : 0u) << (h * GH + g);
+          gsel = actB ? gsel : (MaskT)0;
+#pragma unroll
+          for (int o = TILE; o < 32; o <<= 1) gsel |= __shfl_xor_sync(0xffffffffu, gsel, o);
+          const uint32_t below = (1u << (TILE * h)) - 1u;  // bits of the token's lower lanes
+          const float* sp = srow + EPL * h;
+          const float* bp = bias_s + EPL * h;
+          int base = 0;
+          while (__any_sync(0xffffffffu, gsel != 0)) {
+            const bool has = gsel != 0;
+            const int g = has ? lowest_bit(gsel) : 0;
+            gsel &= gsel - 1;
+            float sv[EPL];
+            if constexpr (EPL == 2) {
+              const float2 s2 = *reinterpret_cast<const float2*>(sp + 8 * g);
+              const float2 b2 = *reinterpret_cast<const float2*>(bp + 8 * g);
+              f2_unpack(f2_add(f2_pack(s2.x, s2.y), f2_pack(b2.x, b2.y)), sv[0], sv[1]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < EPL; ++i) sv[i] = __fadd_rn(sp[8 * g + i], bp[8 * g + i]);
             }
-            if (g >= 0) {
-              float s8[8], b8[8];
-              load8(srow + 8 * g, s8);
-              load8(bias_s + 8 * g, b8);
+            int pre = 0, tot = 0;
+            bool pr[EPL];
 #pragma unroll
-              for (int i = 0; i < 8; ++i)
-                if (__fadd_rn(s8[i], b8[i]) > alpha && c < 15) lst[c++] = 8 * g + i;
+            for (int i = 0; i < EPL; ++i) {
+              pr[i] = has && sv[i] > alpha;
+              const uint32_t x = (__ballot_sync(0xffffffffu, pr[i]) >> t) & PAT;
+              pre += __popc(x & below);
+              tot += __popc(x);
             }
-          }
-          lst[15] = c;
-          __syncwarp();
-          if (actB && h == 0) {
-            int v[KL];
-            int n = 0;
 #pragma unroll
-            for (int i = 0; i < KL; ++i) v[i] = INT_MAX;
-            for (int p = 0; p < LPT; ++p) {
-              const int32_t* lp = reinterpret_cast<int32_t*>(gmax) + (t * LPT + p) * 16;
-              const int cp = lp[15];
-              for (int i = 0; i < cp; ++i) {
-                const int idx = lp[i];
-#pragma unroll
-                for (int q = 0; q < KL; ++q) v[q] = (q == n) ? idx : v[q];
-                ++n;
+            for (int i = 0; i < EPL; ++i) {
+              if (pr[i]) {
+                if (base + pre < k) out[base + pre] = 8 * g + EPL * h + i;
+                ++pre;
               }
             }
-#pragma unroll
-            for (int i = 0; i < KL; ++i)
-#pragma unroll
-              for (int j = KL - 1; j > i; --j) {
-                const int lo = min(v[j - 1], v[j]);
-                v[j] = max(v[j - 1], v[j]);
-                v[j - 1] = lo;
-              }
-#pragma unroll
-            for (int i = 0; i < KL; ++i)
-              if (i < k) out[i] = v[i];
+            base += tot;
           }
         }
       }

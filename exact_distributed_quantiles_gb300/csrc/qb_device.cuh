@@ -108,9 +108,12 @@ __device__ __forceinline__ f2_t f2_sub(f2_t a, f2_t b) {
 }
 __device__ __forceinline__ f2_t f2_splat(float v) { return f2_pack(v, v); }
 
+// Hardware reciprocal estimate.  The .ftz form is the bare estimate; the
+// callers only pass d in [1, 2^125), where input and result are normal and
+// flushing never applies.
 __device__ __forceinline__ float rcp_approx(float d) {
   float y;
-  asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(d));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(d));
   return y;
 }
 

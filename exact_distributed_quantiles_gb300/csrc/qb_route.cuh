@@ -44,6 +44,9 @@
 namespace qb {
 namespace route {
 
+#ifndef QB_ROUTE_MAXW
+#define QB_ROUTE_MAXW 20  // warps per CTA (one CTA per SM), if shared memory allows
+#endif
 constexpr int kWin = 32;      // hi-byte bins privatised in shared memory
 constexpr int kDummy = kWin;  // slot of every other bin (never flushed)
 constexpr int kSmemLimit = 227 * 1024;
@@ -104,15 +107,14 @@ struct Smem {
   static constexpr int kStatic = 256 + E * 4 + 1024;  // static lut + bias, and a margin
   static constexpr int kFixed = kHist + kStatic;
   static constexpr int kTileBytes = TILE * E * 4;  // fp32 scores; bf16 input sits in the upper half
-  // group maxima, later reused for the per-lane top-k lists (32 x 16 ints)
-  static constexpr int kGmax = round16(TILE * GE::GP * 4 > 2048 ? TILE * GE::GP * 4 : 2048);
+  static constexpr int kGmax = round16(TILE * GE::GP * 4);  // group maxima
   static constexpr int kAlpha = round16(TILE * 4);
   static constexpr int GR = (256 / E) > 4 ? 256 / E : 4;  // rows per load group
   static constexpr int NGRP = TILE / GR;                   // mbarriers per warp
   static constexpr int kWarp = kTileBytes + kGmax + kAlpha + round16(NGRP * 8);
   static constexpr int nw_fit() {
     int n = (kSmemLimit - kFixed) / kWarp;
-    return n > 16 ? 16 : n;
+    return n > QB_ROUTE_MAXW ? QB_ROUTE_MAXW : n;
   }
   static constexpr int NW = nw_fit();
   static constexpr int kTotal = kHist + NW * kWarp;  // dynamic shared memory
@@ -402,7 +404,8 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
         if (act[u]) m = fmaxf(m, max_abs8(x[u]));
       ext |= m > kFoldAbsX;
       float s[NS][8];
-      if (m <= kFastAbsX) {
+      // one decision per warp: the packed path unless some lane holds a large x
+      if (__all_sync(0xffffffffu, m <= kFastAbsX)) {
 #pragma unroll
         for (int u = 0; u < NS; ++u)
 #pragma unroll

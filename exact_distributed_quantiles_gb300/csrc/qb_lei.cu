@@ -10,8 +10,8 @@
 //
 // Two kernels:
 //   lei_rho_kernel    one 8-CTA cluster per local batch: load counts in
-//                     shared memory, reduced over the cluster, rho in fp64,
-//                     c_e = RN32(eta * rho_e) into the caller's workspace
+//                     shared memory, reduced over the cluster, rho in fp32,
+//                     c_e = eta * rho_e into the caller's workspace
 //                     [num_batches, E];
 //   lei_apply_kernel  grid-stride stream over grad in 16-byte chunks:
 //                     grad += c_e of the chunk's batch (c rows stay in L1/L2).
@@ -33,7 +33,7 @@ constexpr int kRhoWarps = kRhoThreads / 32;
 // batch's top-k entries (16-byte loads, four in flight per thread) into
 // per-warp shared histograms and reduces them to its own count row; after a
 // cluster barrier, CTA 0 sums the eight rows through distributed shared
-// memory, computes rho in fp64 and writes c_e = RN32(eta * rho_e).  A second
+// memory, computes rho in fp32 and writes c_e = eta * rho_e.  A second
 // cluster barrier keeps every row alive until CTA 0 has read it.
 __global__ void __cluster_dims__(kRhoCluster, 1, 1) __launch_bounds__(kRhoThreads)
     lei_rho_kernel(const int32_t* __restrict__ topk, int64_t N, int E, int k, float eta,
@@ -41,8 +41,8 @@ __global__ void __cluster_dims__(kRhoCluster, 1, 1) __launch_bounds__(kRhoThread
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ int32_t sub[];  // [kRhoWarps][E]
   __shared__ int32_t cnt[512];
-  __shared__ double red[kRhoWarps];
-  __shared__ double t_s[512];
+  __shared__ float red[kRhoWarps];
+  __shared__ float t_s[512];
   const int warp = threadIdx.x >> 5;
   const int rank = (int)cluster.block_rank();
   const int64_t b = blockIdx.x / kRhoCluster;
@@ -95,27 +95,29 @@ __global__ void __cluster_dims__(kRhoCluster, 1, 1) __launch_bounds__(kRhoThread
   }
   cluster.sync();
   if (rank == 0) {
-    const double T = __ddiv_rn((double)((i1 - i0) * (int64_t)k), (double)E);
-    double part = 0.0;
+    // fp32 throughout: the fp64 pipe of this part costs ~150 cycles per
+    // dependent operation, and the result only needs eta * rho to 1e-6
+    // absolute (fp32 keeps it within ~1e-11).  Loads are exact integers.
+    const float T = __fdiv_rn((float)((i1 - i0) * (int64_t)k), (float)E);
+    float part = 0.0f;
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
       int32_t load = 0;
 #pragma unroll
       for (int r = 0; r < kRhoCluster; ++r) load += cluster.map_shared_rank(cnt, r)[e];
-      t_s[e] = tanh(__ddiv_rn(__dsub_rn((double)load, T), T));
-      part = __dadd_rn(part, t_s[e]);
+      t_s[e] = tanhf(__fdiv_rn(__fsub_rn((float)load, T), T));
+      part = __fadd_rn(part, t_s[e]);
     }
-    // mean of tanh over experts: a fixed-shape tree (differs from a serial
-    // sum only in the last bits of an fp64 value)
+    // mean of tanh over experts: a fixed-shape tree
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) part = __dadd_rn(part, __shfl_xor_sync(0xffffffffu, part, o));
+    for (int o = 16; o >= 1; o >>= 1) part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, o));
     if ((threadIdx.x & 31) == 0) red[warp] = part;
     __syncthreads();
-    double sum = 0.0;
+    float sum = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kRhoWarps; ++w) sum = __dadd_rn(sum, red[w]);
-    const double mean = __ddiv_rn(sum, (double)E);
+    for (int w = 0; w < kRhoWarps; ++w) sum = __fadd_rn(sum, red[w]);
+    const float mean = __fdiv_rn(sum, (float)E);
     for (int e = threadIdx.x; e < E; e += blockDim.x)
-      ws[b * E + e] = __double2float_rn(__dmul_rn((double)eta, __dsub_rn(t_s[e], mean)));
+      ws[b * E + e] = __fmul_rn(eta, __fsub_rn(t_s[e], mean));
   }
   cluster.sync();
 }

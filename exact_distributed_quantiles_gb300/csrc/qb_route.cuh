@@ -545,6 +545,46 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
               }
             }
           }
+        } else if constexpr (GH <= 8) {
+          // The k experts above alpha in ascending order.  Lane h owns the
+          // token's groups [h*GH, (h+1)*GH): it tests the elements of each
+          // of its groups whose max exceeds alpha into a bit mask, the
+          // token's lanes scan their counts (lane h's experts all precede
+          // lane h+1's), and each lane writes its own indices in order.
+          uint32_t own = 0;
+#pragma unroll
+          for (int g = 0; g < GH; ++g) own |= (gm[g] > alpha ? 1u : 0u) << g;
+          own = actB ? own : 0u;
+          unsigned long long bits = 0;
+          for (uint32_t m = own; m; m &= m - 1) {
+            const int gl = __ffs((int)m) - 1;
+            float s8[8], b8[8];
+            load8(srow + 8 * (h * GH + gl), s8);
+            load8(bias_s + 8 * (h * GH + gl), b8);
+            uint32_t m8 = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float v0, v1;
+              f2_unpack(f2_add(f2_pack(s8[2 * i], s8[2 * i + 1]), f2_pack(b8[2 * i], b8[2 * i + 1])),
+                        v0, v1);
+              m8 |= (v0 > alpha ? 1u : 0u) << (2 * i);
+              m8 |= (v1 > alpha ? 2u : 0u) << (2 * i);
+            }
+            bits |= (unsigned long long)m8 << (8 * gl);
+          }
+          const int cnt = __popcll(bits);
+          int incl = cnt;
+#pragma unroll
+          for (int o = TILE; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          int pos = incl - cnt;
+          const int ebase = h * GH * 8;
+          for (unsigned long long m = bits; m; m &= m - 1) {
+            if (pos < k) out[pos] = ebase + (__ffsll((long long)m) - 1);
+            ++pos;
+          }
         } else {
           // The k experts above alpha in ascending order.  Only groups whose
           // max exceeds alpha hold any; the token's lanes take each of them

@@ -180,6 +180,9 @@ int k3_finalize(int32_t* hist, int E, int nbins, int64_t r, float* bounds, float
  *   load_e   = #{(i,t) : topk_idx[i,t] == e},   T = n * k / E
  *   rho_raw  = (load_e - T) / T,   rho_e = tanh(rho_raw_e) - mean_e tanh(rho_raw)
  *   grad[i,e] = RN32(grad[i,e] + RN32(eta * rho_e)) for every token i of it.
+ * rho and eta*rho are evaluated in fp32 (loads and T are exact); eta*rho
+ * agrees with the real-number formula to about 1e-11 at eta = 8e-5, well
+ * inside the 1e-6 absolute tolerance on grad.
  *   grad      device fp32 [N, E], updated in place; 16-byte aligned.
  *   topk_idx  device int32 [N, k], entries in [0, E).
  *   workspace device fp32 [num_batches * E] scratch owned by the caller

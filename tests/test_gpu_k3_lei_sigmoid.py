@@ -139,8 +139,11 @@ def test_lei_full_step_microbatches(qb, orc):
         want, load, rho = orc.lei(g0[sl], t[sl], w.eta)
         assert load.sum() == w.n_tokens * w.k
         assert np.max(np.abs(got[sl] - want)) <= LEI_ABS_TOL
+        # the workspace holds eta * rho; the device evaluates rho in fp32
+        # (division, tanh and a 256-term mean: a few ulp of values <= 2), so
+        # eta * rho is within eta * 2e-6 of the fp64 value
         c = ws[m].cpu().numpy()
-        assert np.max(np.abs(c - (np.float32(w.eta) * rho).astype(np.float32))) <= 1e-12
+        assert np.max(np.abs(c.astype(np.float64) - w.eta * rho)) <= w.eta * 2e-6
 
 
 @pytest.mark.parametrize("N,E,k,bt", [(1, 32, 1, 0), (1000, 64, 6, 333), (4097, 512, 15, 1024)])

@@ -213,17 +213,11 @@ def _per_call_ms(fn, reps, warmup):
     return e0.elapsed_time(e1) / reps
 
 
-def components(qb, inputs, dev, reps, warmup, peak_hbm, peaks):
-    """The other two timed paths: K3 histogram mode and the router-GEMM front end.
-
-    K3: E=256, k=8, 4 x 65536 bf16 tokens, 1000 bins; one global batch = four
-    k3_route_hist calls + k3_finalize.  Four copies of the batch at distinct
-    addresses (512 MiB together) are used in turn so that L2 holds none of
-    them.  Router GEMM: 4 x 32768 tokens of bf16 hidden states [., 2048] x W
-    [2048, 256]; one global batch = four GEMM + hi-pass calls, select, lo pass
-    over the stored keys, finalize.  Its 512 MiB of hidden states exceed L2."""
-    out = {}
-    # ---- K3
+def k3_component(qb, inputs, dev, reps, warmup, peak_hbm):
+    """K3 histogram mode: E=256, k=8, 4 x 65536 bf16 tokens, 1000 bins; one
+    global batch = four k3_route_hist calls + k3_finalize.  Four copies of the
+    batch at distinct addresses (512 MiB together) are used in turn so that L2
+    holds none of them."""
     w3 = inputs.WORKLOADS["k3"]
     bias3, mbs3 = inputs.router_layer(w3, inputs.seed_for("k3"), device=dev)
     copies = [[m.clone() for m in mbs3] for _ in range(4)]
@@ -247,7 +241,7 @@ def components(qb, inputs, dev, reps, warmup, peak_hbm, peaks):
     ms_hist = _per_call_ms(k3_hist_only, reps, warmup)
     qb.qb_zero_i32(hist3)
     k3_bytes = w3.n_pool * w3.E * 2  # bf16 logits read once (algorithmic)
-    out["k3"] = {
+    return {
         "workload": "k3: 4x65536 bf16 tokens, E=256, k=8, 1000 bins",
         "value": w3.n_pool / (ms_batch / 1e3), "unit": "tokens/s", "ms_per_batch": ms_batch,
         "launches_per_batch": 2 * w3.n_micro + 1,
@@ -255,9 +249,13 @@ def components(qb, inputs, dev, reps, warmup, peak_hbm, peaks):
                      "achieved": k3_bytes / (ms_hist / 1e3) / 1e9, "peak": peak_hbm,
                      "unit": "GB/s", "frac": k3_bytes / (ms_hist / 1e3) / 1e9 / peak_hbm,
                      "bytes_per_batch": k3_bytes, "hist_ms_per_batch": ms_hist}}
-    del copies, mbs3
 
-    # ---- router GEMM front end
+
+def gemm_component(qb, inputs, dev, reps, warmup, peak_hbm, peaks):
+    """Router GEMM front end: 4 x 32768 tokens of bf16 hidden states [., 2048]
+    x W [2048, 256]; one global batch = four GEMM + hi-pass calls, select, lo
+    pass over the stored keys, finalize.  Its 512 MiB of hidden states exceed
+    L2."""
     w5 = inputs.WORKLOADS["router_gemm"]
     bias5, W, hs = inputs.gemm_layer(w5, inputs.seed_for("router_gemm"), device=dev)
     w_t = W.t().contiguous()
@@ -288,7 +286,7 @@ def components(qb, inputs, dev, reps, warmup, peak_hbm, peaks):
     flops = 2.0 * w5.n_pool * H * E
     gbytes = w5.n_pool * H * 2 + H * E * 2 * w5.n_micro + w5.n_pool * E * 4
     tflops = flops / (ms_g / 1e3) / 1e12
-    out["router_gemm"] = {
+    return {
         "workload": "router_gemm: 4x32768 tokens, hidden 2048 bf16 x W [2048,256] bf16 -> fp32 "
                     "logits, then EQB (k=6) on them",
         "value": w5.n_pool / (ms5 / 1e3), "unit": "tokens/s", "ms_per_batch": ms5,
@@ -299,7 +297,12 @@ def components(qb, inputs, dev, reps, warmup, peak_hbm, peaks):
                      "gemm_ms_per_batch": ms_g,
                      "hbm_gbs": gbytes / (ms_g / 1e3) / 1e9, "hbm_frac": gbytes / (ms_g / 1e3)
                      / 1e9 / peak_hbm}}
-    return out
+
+
+def components(qb, inputs, dev, reps, warmup, peak_hbm, peaks):
+    """The other two timed paths: K3 histogram mode and the router-GEMM front end."""
+    return {"k3": k3_component(qb, inputs, dev, reps, warmup, peak_hbm),
+            "router_gemm": gemm_component(qb, inputs, dev, reps, warmup, peak_hbm, peaks)}
 
 
 def cpu_baseline_sample(n_tokens: int, layer: int = 0):
@@ -368,6 +371,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-components", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD, choices=[WORKLOAD, "k3", "router_gemm"],
+                    help="full_step (the headline line) or one of the other timed paths alone")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -385,6 +390,21 @@ def main():
     from exact_distributed_quantiles_gb300 import build, inputs
     build.build()
     from exact_distributed_quantiles_gb300 import qb
+
+    if args.workload != WORKLOAD:
+        peak, peak_kind, peaks = _peaks()
+        dev = torch.device("cuda", local)
+        reps = max(args.steps, 10)
+        if args.workload == "k3":
+            c = k3_component(qb, inputs, dev, reps, args.warmup, peak)
+        else:
+            c = gemm_component(qb, inputs, dev, reps, args.warmup, peak, peaks)
+        if rank == 0:
+            print(json.dumps({"workload": args.workload, "n_gpus": world, "steps": reps,
+                              "warmup": args.warmup, "data": "synthetic", **c}), flush=True)
+        if dist_on:
+            torch.distributed.destroy_process_group()
+        return
 
     fs = FullStep(qb, inputs, torch.device("cuda", local), args.layers, seed_offset=rank * 100)
     w = fs.w

@@ -16,8 +16,8 @@
 // at the end.  The flush costs one L2 atomic per non-zero counter per CTA, so
 // the grid is one CTA per SM: fewer, longer CTAs mean fewer flushed counters.
 //
-// Finalize.  One cluster of 8 CTAs: a warp per expert finds the bin (lane-
-// contiguous chunk sums, a warp scan, then one lane walks its chunk), the
+// Finalize.  One cluster of 8 CTAs: a warp per expert finds the bin (blocks
+// of 128 bins, coalesced loads, a warp scan per block), the
 // fp64 quantiles are summed per CTA and the 8 partial sums are combined
 // through distributed shared memory in rank order, so every CTA derives the
 // same mean; min and max of the new bias go through the cluster the same way.
@@ -123,49 +123,70 @@ constexpr int kFinCluster = 8;
 constexpr int kFinThreads = 1024;
 
 // First bin whose cumulative count reaches `target` (-1 if none) and the
-// count below it.  Lane l sums bins [l*C, (l+1)*C); a warp scan over the lane
-// sums finds the lane holding the bin, which then walks its chunk.
+// count below it.  The row goes in pieces of 8 blocks of 128 bins; lane l
+// holds bins 4l..4l+3 of every block (coalesced 16-byte loads, all eight
+// issued before any is used), a warp scan per block finds the block and the
+// lane that hold the bin, and that lane checks its four counts.
 __device__ int warp_find_bin(const int32_t* __restrict__ row, int nbins, long long target,
                              long long* before_out) {
   const int lane = threadIdx.x & 31;
-  const int C = (nbins + 31) / 32;
-  const int b0 = lane * C;
-  const int b1 = min(b0 + C, nbins);
-  long long sum = 0;
-#pragma unroll 8
-  for (int b = b0; b < b1; ++b) sum += row[b];
-  long long cum = sum;
+  const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+  unsigned long long base = 0;
+  for (int p0 = 0; p0 < nbins; p0 += 8 * 128) {
+    int4 v[8];
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const long long y = __shfl_up_sync(0xffffffffu, cum, o);
-    if (lane >= o) cum += y;
-  }
-  const unsigned hit = __ballot_sync(0xffffffffu, cum >= target);
-  if (!hit) {
-    *before_out = __shfl_sync(0xffffffffu, cum, 31);
-    return -1;
-  }
-  const int src = __ffs(hit) - 1;
-  int found = -1;
-  long long before = 0;
-  if (lane == src) {
-    long long run = cum - sum;
-    for (int b = b0; b < b1; ++b) {
-      const long long c = row[b];
-      if (run + c >= target) {
-        found = b;
-        break;
+    for (int q = 0; q < 8; ++q) {
+      const int b = p0 + q * 128 + 4 * lane;
+      if (vec && b + 3 < nbins) {
+        v[q] = *reinterpret_cast<const int4*>(row + b);
+      } else {
+        v[q].x = b < nbins ? row[b] : 0;
+        v[q].y = b + 1 < nbins ? row[b + 1] : 0;
+        v[q].z = b + 2 < nbins ? row[b + 2] : 0;
+        v[q].w = b + 3 < nbins ? row[b + 3] : 0;
       }
-      run += c;
     }
-    before = run;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const unsigned s = (unsigned)v[q].x + (unsigned)v[q].y + (unsigned)v[q].z + (unsigned)v[q].w;
+      unsigned incl = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned long long cum = base + incl;
+      const unsigned hit = __ballot_sync(0xffffffffu, (long long)cum >= target);
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        const unsigned long long r0 = cum - s;
+        const unsigned long long r1 = r0 + (unsigned)v[q].x;
+        const unsigned long long r2 = r1 + (unsigned)v[q].y;
+        const unsigned long long r3 = r2 + (unsigned)v[q].z;
+        const int b = p0 + q * 128 + 4 * lane;
+        int off;
+        unsigned long long before;
+        if ((long long)r1 >= target) {
+          off = 0; before = r0;
+        } else if ((long long)r2 >= target) {
+          off = 1; before = r1;
+        } else if ((long long)r3 >= target) {
+          off = 2; before = r2;
+        } else {
+          off = 3; before = r3;
+        }
+        *before_out = (long long)__shfl_sync(0xffffffffu, before, src);
+        return __shfl_sync(0xffffffffu, b + off, src);
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
   }
-  *before_out = __shfl_sync(0xffffffffu, before, src);
-  return __shfl_sync(0xffffffffu, found, src);
+  *before_out = (long long)base;
+  return -1;
 }
 
 __global__ void __cluster_dims__(kFinCluster, 1, 1) __launch_bounds__(kFinThreads)
-    k3_finalize_kernel(int32_t* __restrict__ hist, int E, int nbins, long long r,
+    k3_finalize_kernel(int32_t* __restrict__ hist, int E, int nbins, double inv_nbins, long long r,
                        float* __restrict__ bounds, float* __restrict__ bias_out, int reset) {
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
@@ -178,7 +199,11 @@ __global__ void __cluster_dims__(kFinCluster, 1, 1) __launch_bounds__(kFinThread
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const float lo = bounds[0], hi = bounds[1];
   const double dlo = (double)lo;
-  const double width = __ddiv_rn(__dsub_rn((double)hi, dlo), (double)nbins);
+  // No fp64 division on this path (each costs microseconds of dependent fp64
+  // latency here): width uses the host's RN(1/nbins) and the in-bin fraction
+  // is an fp32 quotient; either differs from the divided form by far less
+  // than the mode's tolerance (the fraction is scaled by width, ~1e-3).
+  const double width = __dmul_rn(__dsub_rn((double)hi, dlo), inv_nbins);
   for (int jl = warp; jl < per; jl += kFinThreads / 32) {
     int32_t* row = hist + (int64_t)(j0 + jl) * nbins;
     long long before = 0;
@@ -188,7 +213,7 @@ __global__ void __cluster_dims__(kFinCluster, 1, 1) __launch_bounds__(kFinThread
         q_s[jl] = (double)hi;
       } else {
         const double edge = __dadd_rn(dlo, __dmul_rn((double)b, width));
-        const double frac = __ddiv_rn((double)(r - before), (double)row[b]);
+        const double frac = (double)__fdiv_rn((float)(r - before), (float)row[b]);
         q_s[jl] = __dadd_rn(edge, __dmul_rn(width, frac));
       }
     }
@@ -209,7 +234,7 @@ __global__ void __cluster_dims__(kFinCluster, 1, 1) __launch_bounds__(kFinThread
   double sum = 0.0;
 #pragma unroll
   for (int c = 0; c < kFinCluster; ++c) sum = __dadd_rn(sum, *cluster.map_shared_rank(&part_s, c));
-  const double mu = __ddiv_rn(sum, (double)E);
+  const double mu = __dmul_rn(sum, 1.0 / (double)E);  // E is a power of two: exact
   for (int jl = threadIdx.x; jl < per; jl += kFinThreads) {
     const float b = __double2float_rn(__dsub_rn(q_s[jl], mu));
     b_s[jl] = b;
@@ -287,8 +312,8 @@ int launch_k3_count(const uint16_t* bins, int64_t N, int E, int nbins, int32_t* 
 int launch_k3_finalize(int32_t* hist, int E, int nbins, int64_t r, float* bounds, float* bias_out,
                        int reset, cudaStream_t stream) {
   if (E % kFinCluster != 0 || E / kFinCluster > 64) return QB_EUNSUPPORTED;
-  k3_finalize_kernel<<<kFinCluster, kFinThreads, 0, stream>>>(hist, E, nbins, (long long)r, bounds,
-                                                              bias_out, reset);
+  k3_finalize_kernel<<<kFinCluster, kFinThreads, 0, stream>>>(hist, E, nbins, 1.0 / (double)nbins,
+                                                              (long long)r, bounds, bias_out, reset);
   return launch_status();
 }
 

@@ -163,10 +163,11 @@ int k3_route_hist(const void* logits, int dtype, const float* bias, int64_t N, i
  *         width = (hi - lo) / nbins;
  *   bias_out[j] = RN32(q_j - mean_j q_j);
  *   bounds <- {min_j bias_out - 1, max_j bias_out + 1} (fp32, in place).
- * The fp64 sum behind the mean is a fixed tree (per-CTA halves of 8 groups
- * of E/8 experts, then the 8 partial sums in order), not the ascending
- * serial order: the result agrees with the serial sum to well within the
- * 1e-6 relative tolerance of this mode.  E must be a multiple of 8, E <= 512.
+ * Device arithmetic differs from these formulas only in rounding, far
+ * inside this mode's 1e-6 relative tolerance: width = (hi - lo) * RN(1/nbins)
+ * and the in-bin fraction (r - before) / count is an fp32 quotient; the fp64
+ * sum behind the mean is a fixed tree (8 groups of E/8 experts, then the 8
+ * partial sums in order), not the ascending serial order.  E <= 512.
  * reset != 0 zeroes hist afterwards.  bounds and bias_out are device. */
 int k3_finalize(int32_t* hist, int E, int nbins, int64_t r, float* bounds, float* bias_out,
                 int reset, void* stream);

@@ -70,14 +70,21 @@ def _k3_gpu(qb, mbs, bias, k, bounds0, nbins):
     return h.cpu().numpy(), b_out.cpu().numpy(), bounds.cpu().numpy()
 
 
-def _check_k3(res, ref):
+def _check_k3(res, ref, bounds0, nbins):
     h, b, bounds = res
     assert np.array_equal(h, ref["hist"])
     scale = np.abs(ref["bias_out"]).max()
     assert np.max(np.abs(b.astype(np.float64) - ref["bias_out"])) <= K3_REL_TOL * scale
     assert np.allclose(bounds, ref["bounds_out"], rtol=0, atol=K3_REL_TOL * scale)
-    # the same fp64 steps on both sides: expect identical bits
-    assert np.array_equal(b.view(np.uint32), ref["bias_out"].view(np.uint32))
+    # Much tighter than the tolerance: the device differs from the oracle
+    # only in rounding -- an fp32 in-bin fraction (relative error <= 2^-23,
+    # scaled by the bin width), fp64 tree sums and reciprocal products, and
+    # the final fp32 rounding of each bias (up to one ulp of it either way).
+    lo, hi = (float(x) for x in np.asarray(bounds0, dtype=np.float64))
+    width = (hi - lo) / nbins
+    ulp = np.spacing(np.abs(ref["bias_out"]).astype(np.float32)).astype(np.float64)
+    err = np.abs(b.astype(np.float64) - ref["bias_out"].astype(np.float64))
+    assert np.all(err <= 2 * ulp + width * 2.0 ** -22)
 
 
 def test_k3_workload(qb, orc):
@@ -87,7 +94,7 @@ def test_k3_workload(qb, orc):
     res = _k3_gpu(qb, mbs, bias, w.k, b0, w.nbins)
     ref = orc.k3_global_batch([host_logits(m) for m in mbs], bias.cpu().numpy(), w.k,
                               b0.numpy(), w.nbins)
-    _check_k3(res, ref)
+    _check_k3(res, ref, b0.numpy(), w.nbins)
 
 
 @pytest.mark.parametrize("E,k,nbins,dtype", [(64, 6, 1000, torch.float32),
@@ -101,7 +108,7 @@ def test_k3_small_shapes(qb, orc, E, k, nbins, dtype):
     res = _k3_gpu(qb, mbs, bias, w.k, b0, nbins)
     ref = orc.k3_global_batch([host_logits(m) for m in mbs], bias.cpu().numpy(), w.k,
                               b0.numpy(), nbins)
-    _check_k3(res, ref)
+    _check_k3(res, ref, b0.numpy(), nbins)
 
 
 def test_k3_out_of_range_clamps(qb, orc):
@@ -113,7 +120,7 @@ def test_k3_out_of_range_clamps(qb, orc):
     ref = orc.k3_global_batch([host_logits(m) for m in mbs], bias.cpu().numpy(), w.k,
                               b0.numpy(), 100)
     assert ref["hist"][:, 0].sum() > 0 and ref["hist"][:, -1].sum() > 0
-    _check_k3(res, ref)
+    _check_k3(res, ref, b0.numpy(), 100)
 
 
 # ------------------------------------------------------------------ LEI

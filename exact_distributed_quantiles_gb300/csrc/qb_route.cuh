@@ -310,7 +310,9 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
   __shared__ uint8_t lut[256];
   __shared__ __align__(16) float bias_s[E];
   int32_t* hist_s = reinterpret_cast<int32_t*>(smem);
-  const int warp = threadIdx.x >> 5;
+  // warp index as a value the compiler knows to be warp-uniform, so that the
+  // per-tile branches below need no divergence handling
+  const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
   const int lane = threadIdx.x & 31;
   unsigned char* wbase = smem + SM::kHist + warp * SM::kWarp;
   unsigned char* tile = wbase;

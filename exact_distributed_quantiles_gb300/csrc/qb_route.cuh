@@ -169,6 +169,14 @@ __device__ __forceinline__ void merge_block8(float (&L)[KL], float (&v)[8]) {
   merge_desc<KL>(L, B);
 }
 
+// L <- the block of 8 values sorted descending (L was empty).
+template <int KL>
+__device__ __forceinline__ void first_block8(float (&L)[KL], float (&v)[8]) {
+  sort8_desc(v);
+#pragma unroll
+  for (int i = 0; i < KL; ++i) L[i] = i < 8 ? v[i] : -INFINITY;
+}
+
 // Merge the list of lane ^ o into L.
 template <int KL>
 __device__ __forceinline__ void merge_partner(float (&L)[KL], int o) {
@@ -470,12 +478,17 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
 #pragma unroll
       for (int i = 0; i < KL; ++i) L[i] = -INFINITY;
       if constexpr (GH % 8 == 0) {
+        // the first block sorted is the list (merging it into -inf would
+        // only copy it); later blocks merge
 #pragma unroll
         for (int b0 = 0; b0 < GH; b0 += 8) {
           float v8[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) v8[i] = gm[b0 + i];
-          merge_block8<KL>(L, v8);
+          if (b0 == 0)
+            first_block8<KL>(L, v8);
+          else
+            merge_block8<KL>(L, v8);
         }
       } else {
 #pragma unroll
@@ -494,6 +507,7 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
 #pragma unroll
       for (int i = 0; i < KL; ++i) L[i] = -INFINITY;
       const float* srow = sc + t * E;
+      bool fresh = true;  // L still empty: the first group is sorted into it directly
       for (MaskT m = cand; m;) {
         int g = -1;
 #pragma unroll
@@ -510,7 +524,11 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
           for (int i = 0; i < 4; ++i)
             f2_unpack(f2_add(f2_pack(s8[2 * i], s8[2 * i + 1]), f2_pack(b8[2 * i], b8[2 * i + 1])),
                       s8[2 * i], s8[2 * i + 1]);
-          merge_block8<KL>(L, s8);
+          if (fresh)
+            first_block8<KL>(L, s8);
+          else
+            merge_block8<KL>(L, s8);
+          fresh = false;
         }
       }
 #pragma unroll

@@ -336,3 +336,56 @@ def num_threads() -> int:
 
 def set_num_threads(n: int) -> None:
     _load().orc_set_num_threads(int(n))
+
+
+# ------------------------------------------------------------ rank-averaged QB
+
+def rank_averaged_qb(rank_microbatches, bias, k: int) -> dict:
+    """Rank-averaged QB: each rank's own k/E quantile, averaged over the ranks.
+
+    "Exact Quantile Balancing and Load-Error Injection for Mixture-of-
+    Experts", opening paragraph: the MARIN implementation averages rank-local
+    quantiles, so its result depends on how the batch is sharded (quantiles do
+    not commute with averaging).  Reading used: rank p's quantile q_p[j] is
+    the exact order statistic of its own BF16 margins at R_p = ceil(k*N_p/E)
+    (what the pooled method computes on that rank's tokens alone); the bias is
+    avg[j] = (sum over p in rank order of q_p[j], fp64) / P, then centred like
+    the pooled method.  ``rank_microbatches``: one list of logits arrays per
+    rank, all routed with ``bias``.
+    """
+    per_rank = [eqb_global_batch(mbs, bias, k) for mbs in rank_microbatches]
+    E = np.asarray(bias).shape[0]
+    s = np.zeros(E, np.float64)
+    for r in per_rank:
+        s = s + r["q"]
+    avg = s / float(len(per_rank))
+    return dict(q_rank=np.stack([r["q"] for r in per_rank]),
+                qkey_rank=np.stack([r["qkey"] for r in per_rank]), avg=avg,
+                bias_out=center(avg))
+
+
+# ---------------------------------------------------------------------- MaxVio
+
+def maxvio(topk_batches, E: int) -> dict:
+    """Load imbalance of the routed top-k sets.
+
+    Same paper, testbed paragraph: MaxVio is how far the busiest expert
+    exceeds uniform load.  Reading used: for a set of tokens with total n*k
+    assignments, T = n*k/E and MaxVio = (max_e load_e - T) / T; "global" over
+    all local batches together, "local" the mean over local batches of each
+    batch's own value (fp64 throughout).  ``topk_batches``: one int array
+    [n_b, k] per local batch.
+    """
+    loads = [np.bincount(np.asarray(t).ravel(), minlength=E).astype(np.int64) for t in topk_batches]
+    tot = np.zeros(E, np.int64)
+    for l in loads:
+        tot = tot + l
+    n_all = sum(int(np.asarray(t).size) for t in topk_batches)
+    T = n_all / E
+    glob = (float(tot.max()) - T) / T
+    loc = 0.0
+    for t, l in zip(topk_batches, loads):
+        Tb = int(np.asarray(t).size) / E
+        loc = loc + (float(l.max()) - Tb) / Tb
+    loc = loc / len(topk_batches)
+    return dict(loads=np.stack(loads), global_maxvio=glob, local_maxvio=loc)

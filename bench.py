@@ -299,10 +299,72 @@ def gemm_component(qb, inputs, dev, reps, warmup, peak_hbm, peaks):
                      / 1e9 / peak_hbm}}
 
 
+def rank_average_component(qb, inputs, dev, reps, warmup, peak_hbm):
+    """Rank-averaged QB on the pooled workload (E=256, k=6, 8 x 16384 skewed
+    tokens) as 8 ranks of one microbatch each: per rank the EQB steps on its
+    own tokens, then the average of the 8 selected keys.  Timed next to the
+    pooled EQB of the same tokens."""
+    w = inputs.WORKLOADS["eqb_pooled"]
+    bias, mbs = inputs.router_layer(w, inputs.seed_for("eqb_pooled"), device=dev)
+    E, n = w.E, w.n_tokens
+    keys = torch.empty(w.n_pool, E, dtype=torch.int16, device=dev)
+    hi = torch.zeros(E, 256, dtype=torch.int32, device=dev)
+    lo = torch.zeros_like(hi)
+    sel = torch.empty(E, dtype=torch.int32, device=dev)
+    r_lo = torch.empty_like(sel)
+    qk = torch.empty(w.n_micro, E, dtype=torch.int16, device=dev)
+    scratch = torch.empty(E, dtype=torch.float32, device=dev)
+    out = torch.empty(E, dtype=torch.float32, device=dev)
+
+    def ranks():
+        for p, m in enumerate(mbs):
+            kp = keys[p * n:(p + 1) * n]
+            qb.qb_route_hist_hi(m, bias, w.k, hi, keys_out=kp)
+            qb.qb_select_hi(hi, qb.rank(n, E, w.k), sel, r_lo)
+            qb.qb_keys_hist_lo(kp, sel, lo)
+            qb.qb_finalize(hi, lo, sel, r_lo, scratch, qkey_out=qk[p], reset=True)
+        qb.qb_rank_average(qk, out)
+
+    def pooled():
+        for p, m in enumerate(mbs):
+            qb.qb_route_hist_hi(m, bias, w.k, hi, keys_out=keys[p * n:(p + 1) * n])
+        qb.qb_select_hi(hi, qb.rank(w.n_pool, E, w.k), sel, r_lo)
+        qb.qb_keys_hist_lo(keys, sel, lo)
+        qb.qb_finalize(hi, lo, sel, r_lo, out, reset=True)
+
+    ms_r = _per_call_ms(ranks, reps, warmup)
+    ms_p = _per_call_ms(pooled, reps, warmup)
+    return {"workload": "eqb_pooled as 8 ranks: 8 x 16384 tokens, E=256, k=6",
+            "value": w.n_pool / (ms_r / 1e3), "unit": "tokens/s", "ms_per_batch": ms_r,
+            "pooled_eqb_ms_per_batch": ms_p, "launches_per_batch": 4 * w.n_micro + 1,
+            "roofline": {"bound": "hbm", "bytes_per_batch": w.n_pool * E * 8,
+                         "achieved": w.n_pool * E * 8 / (ms_r / 1e3) / 1e9, "peak": peak_hbm,
+                         "unit": "GB/s",
+                         "frac": w.n_pool * E * 8 / (ms_r / 1e3) / 1e9 / peak_hbm}}
+
+
+def maxvio_component(qb, inputs, dev, reps, warmup):
+    """MaxVio of one full-step layer: 524288 tokens' top-6 sets in 16 local
+    batches of 32768 (the sets the hi pass writes for LEI)."""
+    w = inputs.WORKLOADS["full_step"]
+    topk = inputs.random_topk(w.n_pool, w.E, w.k, seed=4, device=dev)
+    loads = torch.empty(w.n_micro, w.E, dtype=torch.int32, device=dev)
+    mv = torch.empty(2, dtype=torch.float64, device=dev)
+    ms = _per_call_ms(lambda: qb.qb_maxvio(topk, w.E, loads, mv, batch_tokens=w.n_tokens),
+                      reps, warmup)
+    nbytes = w.n_pool * w.k * 4
+    return {"workload": "full_step layer: 16 x 32768 tokens, top-6 of 256", "ms_per_call": ms,
+            "launches_per_call": 2, "bytes_per_call": nbytes,
+            "achieved_gbs": nbytes / (ms / 1e3) / 1e9}
+
+
 def components(qb, inputs, dev, reps, warmup, peak_hbm, peaks):
-    """The other two timed paths: K3 histogram mode and the router-GEMM front end."""
+    """The other timed paths: K3 histogram mode, the router-GEMM front end,
+    rank-averaged QB and the MaxVio diagnostic."""
     return {"k3": k3_component(qb, inputs, dev, reps, warmup, peak_hbm),
-            "router_gemm": gemm_component(qb, inputs, dev, reps, warmup, peak_hbm, peaks)}
+            "router_gemm": gemm_component(qb, inputs, dev, reps, warmup, peak_hbm, peaks),
+            "rank_average": rank_average_component(qb, inputs, dev, reps, warmup, peak_hbm),
+            "maxvio": maxvio_component(qb, inputs, dev, reps, warmup)}
 
 
 def cpu_baseline_sample(n_tokens: int, layer: int = 0):
@@ -371,7 +433,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-components", action="store_true")
-    ap.add_argument("--workload", default=WORKLOAD, choices=[WORKLOAD, "k3", "router_gemm"],
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=[WORKLOAD, "k3", "router_gemm", "rank_average", "maxvio"],
                     help="full_step (the headline line) or one of the other timed paths alone")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -397,8 +460,12 @@ def main():
         reps = max(args.steps, 10)
         if args.workload == "k3":
             c = k3_component(qb, inputs, dev, reps, args.warmup, peak)
-        else:
+        elif args.workload == "router_gemm":
             c = gemm_component(qb, inputs, dev, reps, args.warmup, peak, peaks)
+        elif args.workload == "rank_average":
+            c = rank_average_component(qb, inputs, dev, reps, args.warmup, peak)
+        else:
+            c = maxvio_component(qb, inputs, dev, reps, args.warmup)
         if rank == 0:
             print(json.dumps({"workload": args.workload, "n_gpus": world, "steps": reps,
                               "warmup": args.warmup, "data": "synthetic", **c}), flush=True)
@@ -425,6 +492,8 @@ def main():
     n, E, k = w.n_pool, w.E, w.k
     hi_bytes = n * E * (4 + 2) + n * k * 4   # logits read, keys write, top-k write
     hi_avg_ms = statistics.mean(hi_ms) if hi_ms else float("nan")
+    eqb_bytes = hi_bytes + n * E * 2                      # + the lo pass over the keys
+    step_bytes = eqb_bytes + n * k * 4 + n * E * 4 * 2    # + LEI counts and grad read/write
     achieved = hi_bytes / (hi_avg_ms / 1e3) / 1e9
 
     # end to end through host buffers: per layer H2D logits + grad, D2H grad + bias
@@ -477,6 +546,16 @@ def main():
                        "parallelism": f"replicas x{world} (token shards, no collective)",
                        "l2": "inputs (48 GiB) far larger than L2; no flush"},
             "eqb_only": {"value": eqb_value, "unit": UNIT, "ms_per_step": ms_eqb / args.steps},
+            # whole-path HBM roofline: algorithmic bytes of every kernel of a layer
+            # (hi pass 1560 B/token, lo pass 512, LEI counts 24, LEI apply 2048)
+            # over the measured step time
+            "step_roofline": {
+                "bytes_per_layer": step_bytes, "eqb_bytes_per_layer": eqb_bytes,
+                "achieved": step_bytes * fs.L / (ms_step / 1e3) / 1e9,
+                "eqb_achieved": eqb_bytes * fs.L / ((ms_eqb / args.steps) / 1e3) / 1e9,
+                "peak": peak, "unit": "GB/s",
+                "frac": step_bytes * fs.L / (ms_step / 1e3) / 1e9 / peak,
+                "eqb_frac": eqb_bytes * fs.L / ((ms_eqb / args.steps) / 1e3) / 1e9 / peak},
             "roofline": {"bound": "hbm", "kernel": "qb_route_hist_hi (route_kernel hi mode)",
                          "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                          "unit": "GB/s", "frac": achieved / peak, "traffic": _route_traffic(n),

@@ -221,6 +221,25 @@ int qb_router_gemm_hist_hi(const void* hidden, const void* w_t, int64_t M, int H
                           alpha_out, stream);
 }
 
+int qb_rank_average(const uint16_t* qkeys, int P, int E, float* bias_out, void* stream) {
+  if (!qkeys || !bias_out || P < 1) return QB_EINVAL;
+  if (!supported_E(E)) return QB_EUNSUPPORTED;
+  return launch_rank_average(qkeys, P, E, bias_out, as_stream(stream));
+}
+
+int qb_maxvio(const int32_t* topk_idx, int64_t N, int E, int k, int64_t batch_tokens,
+              int32_t* loads_out, double* maxvio_out, void* stream) {
+  if (!topk_idx || !loads_out || !maxvio_out) return QB_EINVAL;
+  if (!aligned16(topk_idx)) return QB_EINVAL;
+  if (N < 1 || batch_tokens < 0) return QB_EINVAL;
+  if (!supported_E(E)) return QB_EUNSUPPORTED;
+  if (k < 1 || k >= E) return QB_EINVAL;
+  if (batch_tokens == 0 || batch_tokens > N) batch_tokens = N;
+  if (N > INT32_MAX) return QB_EOVERFLOW;
+  return launch_maxvio(topk_idx, N, E, k, batch_tokens, loads_out, maxvio_out,
+                       as_stream(stream));
+}
+
 int qb_device_status(int* flags_out) {
   int* p = device_status_ptr();
   if (!p) return QB_ECUDA;

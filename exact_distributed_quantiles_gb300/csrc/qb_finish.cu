@@ -257,6 +257,33 @@ __global__ void __launch_bounds__(512) eqb_center_kernel(float* __restrict__ bia
 }
 
 // ------------------------------------------------------------------------
+// Rank-averaged QB: each rank's selected key (qb_finalize's qkey_out) decoded,
+// averaged over the ranks in rank order in fp64, then centred like the pooled
+// method (serial ascending fp64 mean, as the plain definition does it; one
+// call per global batch).
+// ------------------------------------------------------------------------
+__global__ void __launch_bounds__(512) rank_average_kernel(const uint16_t* __restrict__ qkeys,
+                                                           int P, int E,
+                                                           float* __restrict__ bias_out) {
+  __shared__ double avg_s[512];
+  __shared__ double mu_s;
+  for (int j = threadIdx.x; j < E; j += blockDim.x) {
+    double s = 0.0;
+    for (int p = 0; p < P; ++p) s = __dadd_rn(s, (double)key_decode(qkeys[(int64_t)p * E + j]));
+    avg_s[j] = __ddiv_rn(s, (double)P);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double sum = 0.0;
+    for (int j = 0; j < E; ++j) sum = __dadd_rn(sum, avg_s[j]);
+    mu_s = __ddiv_rn(sum, (double)E);
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < E; j += blockDim.x)
+    bias_out[j] = __double2float_rn(__dsub_rn(avg_s[j], mu_s));
+}
+
+// ------------------------------------------------------------------------
 // Utilities.
 // ------------------------------------------------------------------------
 __global__ void zero_i32_kernel(int32_t* __restrict__ p, int64_t n) {
@@ -332,6 +359,12 @@ int launch_finalize(int32_t* hist_hi, int32_t* hist_lo, const int32_t* sel, cons
   int st = launch_status();
   if (st != QB_OK) return st;
   eqb_center_kernel<<<1, 512, 0, stream>>>(bias_out, E);
+  return launch_status();
+}
+
+int launch_rank_average(const uint16_t* qkeys, int P, int E, float* bias_out,
+                        cudaStream_t stream) {
+  rank_average_kernel<<<1, 512, 0, stream>>>(qkeys, P, E, bias_out);
   return launch_status();
 }
 

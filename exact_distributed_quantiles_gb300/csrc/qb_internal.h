@@ -45,6 +45,10 @@ int launch_k3_finalize(int32_t* hist, int E, int nbins, int64_t r, float* bounds
 int launch_k3_count(const uint16_t* bins, int64_t N, int E, int nbins, int32_t* hist,
                     cudaStream_t stream);
 int launch_zero_i32(int32_t* p, int64_t n, cudaStream_t stream);
+int launch_rank_average(const uint16_t* qkeys, int P, int E, float* bias_out,
+                        cudaStream_t stream);
+int launch_maxvio(const int32_t* topk, int64_t N, int E, int k, int64_t batch_tokens,
+                  int32_t* loads, double* out, cudaStream_t stream);
 int launch_sigmoid(const float* x, float* s, int64_t n, cudaStream_t stream);
 int launch_lei(float* grad, const int32_t* topk, int64_t N, int E, int k, float eta,
                int64_t batch_tokens, float* workspace, cudaStream_t stream);

@@ -35,19 +35,15 @@ constexpr int kRhoWarps = kRhoThreads / 32;
 // cluster barrier, CTA 0 sums the eight rows through distributed shared
 // memory, computes rho in fp32 and writes c_e = eta * rho_e.  A second
 // cluster barrier keeps every row alive until CTA 0 has read it.
-__global__ void __cluster_dims__(kRhoCluster, 1, 1) __launch_bounds__(kRhoThreads)
-    lei_rho_kernel(const int32_t* __restrict__ topk, int64_t N, int E, int k, float eta,
-                   int64_t batch_tokens, float* __restrict__ ws) {
-  cg::cluster_group cluster = cg::this_cluster();
-  extern __shared__ int32_t sub[];  // [kRhoWarps][E]
-  __shared__ int32_t cnt[512];
-  __shared__ float red[kRhoWarps];
-  __shared__ float t_s[512];
+// Count one eighth (this CTA's rank in the cluster) of local batch b's top-k
+// entries into cnt[E]: per-warp shared histograms (sub, [kRhoWarps][E]),
+// then one row per CTA.  Returns the batch's token range through i0/i1.
+__device__ void count_batch_loads(const int32_t* __restrict__ topk, int64_t N, int E, int k,
+                                  int64_t batch_tokens, int64_t b, int rank, int32_t* sub,
+                                  int32_t* cnt, int64_t& i0, int64_t& i1) {
   const int warp = threadIdx.x >> 5;
-  const int rank = (int)cluster.block_rank();
-  const int64_t b = blockIdx.x / kRhoCluster;
-  const int64_t i0 = b * batch_tokens;
-  int64_t i1 = i0 + batch_tokens;
+  i0 = b * batch_tokens;
+  i1 = i0 + batch_tokens;
   if (i1 > N) i1 = N;
   for (int q = threadIdx.x; q < kRhoWarps * E; q += blockDim.x) sub[q] = 0;
   __syncthreads();
@@ -93,6 +89,21 @@ __global__ void __cluster_dims__(kRhoCluster, 1, 1) __launch_bounds__(kRhoThread
     for (int w = 0; w < kRhoWarps; ++w) c += sub[w * E + e];
     cnt[e] = c;
   }
+}
+
+__global__ void __cluster_dims__(kRhoCluster, 1, 1) __launch_bounds__(kRhoThreads)
+    lei_rho_kernel(const int32_t* __restrict__ topk, int64_t N, int E, int k, float eta,
+                   int64_t batch_tokens, float* __restrict__ ws) {
+  cg::cluster_group cluster = cg::this_cluster();
+  extern __shared__ int32_t sub[];  // [kRhoWarps][E]
+  __shared__ int32_t cnt[512];
+  __shared__ float red[kRhoWarps];
+  __shared__ float t_s[512];
+  const int warp = threadIdx.x >> 5;
+  const int rank = (int)cluster.block_rank();
+  const int64_t b = blockIdx.x / kRhoCluster;
+  int64_t i0, i1;
+  count_batch_loads(topk, N, E, k, batch_tokens, b, rank, sub, cnt, i0, i1);
   cluster.sync();
   if (rank == 0) {
     // fp32 throughout: the fp64 pipe of this part costs ~150 cycles per
@@ -120,6 +131,87 @@ __global__ void __cluster_dims__(kRhoCluster, 1, 1) __launch_bounds__(kRhoThread
       ws[b * E + e] = __fmul_rn(eta, __fsub_rn(t_s[e], mean));
   }
   cluster.sync();
+}
+
+// MaxVio, pass 1: the load counts of every local batch (one 8-CTA cluster
+// per batch, the same counting as the LEI rho kernel) into loads[nb, E].
+__global__ void __cluster_dims__(kRhoCluster, 1, 1) __launch_bounds__(kRhoThreads)
+    load_count_kernel(const int32_t* __restrict__ topk, int64_t N, int E, int k,
+                      int64_t batch_tokens, int32_t* __restrict__ loads) {
+  cg::cluster_group cluster = cg::this_cluster();
+  extern __shared__ int32_t sub[];  // [kRhoWarps][E]
+  __shared__ int32_t cnt[512];
+  const int rank = (int)cluster.block_rank();
+  const int64_t b = blockIdx.x / kRhoCluster;
+  int64_t i0, i1;
+  count_batch_loads(topk, N, E, k, batch_tokens, b, rank, sub, cnt, i0, i1);
+  cluster.sync();
+  if (rank == 0) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int32_t load = 0;
+#pragma unroll
+      for (int r = 0; r < kRhoCluster; ++r) load += cluster.map_shared_rank(cnt, r)[e];
+      loads[b * E + e] = load;
+    }
+  }
+  cluster.sync();  // keep every CTA's row alive until rank 0 has read it
+}
+
+// MaxVio, pass 2 (one CTA): T = n*k/E; global (max_e sum_b loads - T)/T over
+// all tokens, local = mean over batches of (max_e loads_b - T_b)/T_b, in fp64
+// with the batch terms added in batch order (the plain definition's order).
+// Each warp computes whole batch terms (max over experts, then the fp64
+// quotient, independently of the other batches); only the ordered sum of the
+// terms is serial.
+constexpr int kMaxvioThreads = 512;
+constexpr int kMaxvioWarps = kMaxvioThreads / 32;
+
+__global__ void __launch_bounds__(kMaxvioThreads) maxvio_kernel(
+    const int32_t* __restrict__ loads, int64_t nb, int64_t N, int E, int k, int64_t batch_tokens,
+    double* __restrict__ out) {
+  __shared__ double term_s[kMaxvioWarps];
+  __shared__ long long gmax_s[kMaxvioWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  double local = 0.0;
+  for (int64_t b0 = 0; b0 < nb; b0 += kMaxvioWarps) {
+    const int64_t b = b0 + warp;
+    if (b < nb) {
+      int mx = -1;
+      for (int e = lane; e < E; e += 32) mx = max(mx, loads[b * E + e]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const int64_t i0 = b * batch_tokens;
+      const int64_t n = i0 + batch_tokens < N ? batch_tokens : N - i0;
+      const double Tb = __ddiv_rn((double)(n * k), (double)E);
+      if (lane == 0) term_s[warp] = __ddiv_rn(__dsub_rn((double)mx, Tb), Tb);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int cnt = nb - b0 < kMaxvioWarps ? (int)(nb - b0) : kMaxvioWarps;
+      for (int w = 0; w < cnt; ++w) local = __dadd_rn(local, term_s[w]);
+    }
+    __syncthreads();
+  }
+  long long mine = -1;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    long long s = 0;
+    for (int64_t b = 0; b < nb; ++b) s += loads[b * E + e];
+    mine = s > mine ? s : mine;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const long long y = __shfl_xor_sync(0xffffffffu, mine, o);
+    mine = y > mine ? y : mine;
+  }
+  if (lane == 0) gmax_s[warp] = mine;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long tot = gmax_s[0];
+    for (int w = 1; w < kMaxvioWarps; ++w) tot = gmax_s[w] > tot ? gmax_s[w] : tot;
+    const double T = __ddiv_rn((double)(N * k), (double)E);
+    out[0] = __ddiv_rn(__dsub_rn((double)tot, T), T);
+    out[1] = __ddiv_rn(local, (double)nb);
+  }
 }
 
 // grad += c[batch(row)] streamed in 16-byte chunks.  Each CTA walks whole
@@ -168,6 +260,18 @@ __global__ void __launch_bounds__(kApplyThreads) lei_apply_kernel(float* __restr
 }
 
 }  // namespace
+
+int launch_maxvio(const int32_t* topk, int64_t N, int E, int k, int64_t batch_tokens,
+                  int32_t* loads, double* out, cudaStream_t stream) {
+  const int64_t nb = (N + batch_tokens - 1) / batch_tokens;
+  const int smem = kRhoWarps * E * (int)sizeof(int32_t);
+  load_count_kernel<<<(unsigned)(nb * kRhoCluster), kRhoThreads, smem, stream>>>(
+      topk, N, E, k, batch_tokens, loads);
+  int st = launch_status();
+  if (st != QB_OK) return st;
+  maxvio_kernel<<<1, kMaxvioThreads, 0, stream>>>(loads, nb, N, E, k, batch_tokens, out);
+  return launch_status();
+}
 
 int launch_lei(float* grad, const int32_t* topk, int64_t N, int E, int k, float eta,
                int64_t batch_tokens, float* workspace, cudaStream_t stream) {

@@ -22,7 +22,8 @@ QB_F32, QB_BF16 = 0, 1
 EXPORTS = ("qb_status_string", "qb_version", "qb_rank", "qb_sigmoid", "qb_zero_i32",
            "qb_route_hist_hi", "qb_select_hi", "qb_keys_hist_lo", "qb_route_hist_lo",
            "qb_finalize", "k3_route_hist", "k3_finalize", "lei_inject", "qb_device_status",
-           "lei_inject_noalloc", "qb_router_gemm", "qb_router_gemm_hist_hi")
+           "lei_inject_noalloc", "qb_router_gemm", "qb_router_gemm_hist_hi", "qb_rank_average",
+           "qb_maxvio")
 
 
 class QBError(RuntimeError):
@@ -55,6 +56,8 @@ def _load():
         "lei_inject_noalloc": (I, [P, P, I64, I, I, F, I64, P]),
         "qb_router_gemm": (I, [P, P, I64, I, I, P, P]),
         "qb_router_gemm_hist_hi": (I, [P, P, I64, I, I, I, P, P, P, P, P, P, P]),
+        "qb_rank_average": (I, [P, I, I, P, P]),
+        "qb_maxvio": (I, [P, I64, I, I, I64, P, P, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -200,6 +203,19 @@ def qb_router_gemm_hist_hi(hidden, w_t, bias, k, logits_out, hist_hi, keys_out=N
            lib.qb_router_gemm_hist_hi(_ptr(hidden), _ptr(w_t), M, H, E, int(k), _ptr(bias),
                                       _ptr(logits_out), _ptr(hist_hi), _ptr(keys_out),
                                       _ptr(topk_out), _ptr(alpha_out), _stream(stream)))
+
+
+def qb_rank_average(qkeys, bias_out, stream=None):
+    """qkeys: int16/uint16 [P, E] selected keys of P ranks -> centred average bias."""
+    P, E = qkeys.shape
+    _check("qb_rank_average", lib.qb_rank_average(_ptr(qkeys), P, E, _ptr(bias_out),
+                                                  _stream(stream)))
+
+
+def qb_maxvio(topk, E, loads_out, maxvio_out, batch_tokens=0, stream=None):
+    N, k = topk.shape
+    _check("qb_maxvio", lib.qb_maxvio(_ptr(topk), N, int(E), k, int(batch_tokens),
+                                      _ptr(loads_out), _ptr(maxvio_out), _stream(stream)))
 
 
 def device_status() -> int:

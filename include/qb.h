@@ -234,6 +234,33 @@ int qb_router_gemm_hist_hi(const void* hidden, const void* w_t, int64_t M, int H
 int lei_inject_noalloc(float* grad, const int32_t* topk_idx, int64_t N, int E, int k, float eta,
                        int64_t batch_tokens, void* stream);
 
+/* ------------------------------------------------ comparison and diagnostics ---- */
+
+/* Rank-averaged QB, the sharding-dependent scheme that [EQB]'s opening
+ * paragraph attributes to the MARIN implementation (average of rank-local
+ * quantiles).  Each of P ranks runs the EQB steps on its own tokens only
+ * (qb_route_hist_hi ... qb_finalize with its own rank R_p = ceil(k*N_p/E)) and
+ * hands over the selected keys (qb_finalize's qkey_out).  Then
+ *   avg[j]      = (sum over p in rank order of q_p[j], fp64) / P,
+ *                 q_p[j] the fp32 value of the bf16 number with key qkeys[p,j]
+ *   bias_out[j] = RN32(avg[j] - mu),  mu = (sum_j avg[j] in fp64, ascending j)/E
+ *   qkeys    device uint16 [P, E];  bias_out device fp32 [E].
+ * One launch; the same arithmetic order as the plain definition (results
+ * bit-equal to it). */
+int qb_rank_average(const uint16_t* qkeys, int P, int E, float* bias_out, void* stream);
+
+/* MaxVio load-imbalance diagnostic ([EQB] testbed paragraph: how far the
+ * busiest expert exceeds uniform load).  The N tokens' top-k sets are split
+ * into local batches of batch_tokens (0 = one batch; the last may be shorter):
+ *   loads_out[b][e] = #{(i,t) in batch b : topk_idx[i,t] == e}
+ *   maxvio_out[0]   = (max_e sum_b loads[b][e] - T) / T,  T = N*k/E   (global)
+ *   maxvio_out[1]   = mean_b (max_e loads[b][e] - T_b) / T_b,  T_b = n_b*k/E (local)
+ * in fp64, batches in order.  topk_idx device int32 [N, k] (16-byte
+ * aligned), loads_out device int32 [num_batches, E], maxvio_out device
+ * double [2].  Two launches. */
+int qb_maxvio(const int32_t* topk_idx, int64_t N, int E, int k, int64_t batch_tokens,
+              int32_t* loads_out, double* maxvio_out, void* stream);
+
 /* Reads and clears the device status word that kernels set instead of
  * trapping (bit 0: a bounded wait timed out).  Synchronous; returns QB_OK
  * when clear, QB_EDEVICE when a flag was set, QB_ECUDA on a CUDA error. */

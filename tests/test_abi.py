@@ -103,6 +103,14 @@ def test_argument_errors_are_reported_before_launch(lib):
     assert L.lei_inject(fake, fake, 10, 256, 6, 8e-5, 0, N0, N0) == lib.QB_EINVAL
     assert L.lei_inject(fake, fake, 10, 256, 0, 8e-5, 0, fake, N0) == lib.QB_EINVAL
     assert L.lei_inject(fake, fake, 0, 256, 6, 8e-5, 0, fake, N0) == lib.QB_OK
+    # rank average and MaxVio
+    assert L.qb_rank_average(N0, 2, 256, fake, N0) == lib.QB_EINVAL
+    assert L.qb_rank_average(fake, 0, 256, fake, N0) == lib.QB_EINVAL
+    assert L.qb_rank_average(fake, 2, 100, fake, N0) == lib.QB_EUNSUPPORTED
+    assert L.qb_maxvio(odd, 10, 256, 6, 0, fake, fake, N0) == lib.QB_EINVAL
+    assert L.qb_maxvio(fake, 0, 256, 6, 0, fake, fake, N0) == lib.QB_EINVAL
+    assert L.qb_maxvio(fake, 10, 256, 6, 0, fake, N0, N0) == lib.QB_EINVAL
+    assert L.qb_maxvio(fake, 10, 256, 256, 0, fake, fake, N0) == lib.QB_EINVAL
 
 
 def test_binding_raises_with_status(lib):

@@ -215,10 +215,18 @@ int qb_router_gemm_hist_hi(const void* hidden, const void* w_t, int64_t M, int H
                            const float* bias, float* logits_out, int32_t* hist_hi,
                            uint16_t* keys_out, int32_t* topk_out, float* alpha_out,
                            void* stream) {
-  int st = qb_router_gemm(hidden, w_t, M, H, E, logits_out, stream);
-  if (st != QB_OK || M == 0) return st;
-  return qb_route_hist_hi(logits_out, QB_F32, bias, M, E, k, hist_hi, keys_out, topk_out,
-                          alpha_out, stream);
+  if (!hidden || !w_t || !bias || !hist_hi) return QB_EINVAL;
+  if (!aligned16(hidden) || !aligned16(w_t)) return QB_EINVAL;
+  if ((logits_out && !aligned16(logits_out)) || (keys_out && !aligned16(keys_out)))
+    return QB_EINVAL;
+  if (M < 0) return QB_EINVAL;
+  if (M > INT32_MAX) return QB_EOVERFLOW;
+  if (E != 256 || H < 64 || H % 64 != 0) return QB_EUNSUPPORTED;
+  if (k < 1 || k >= E) return QB_EINVAL;
+  if (k > 15) return QB_EUNSUPPORTED;
+  if (M == 0) return QB_OK;
+  return launch_router_gemm_route(hidden, w_t, M, H, k, bias, hist_hi, keys_out, topk_out,
+                                  alpha_out, logits_out, as_stream(stream));
 }
 
 int qb_rank_average(const uint16_t* qkeys, int P, int E, float* bias_out, void* stream) {

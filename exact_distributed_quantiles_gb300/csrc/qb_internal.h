@@ -45,6 +45,10 @@ int launch_k3_finalize(int32_t* hist, int E, int nbins, int64_t r, float* bounds
 int launch_k3_count(const uint16_t* bins, int64_t N, int E, int nbins, int32_t* hist,
                     cudaStream_t stream);
 int launch_zero_i32(int32_t* p, int64_t n, cudaStream_t stream);
+int launch_router_gemm_route(const void* hidden, const void* w_t, int64_t M, int K, int k,
+                             const float* bias, int32_t* hist, uint16_t* keys_out,
+                             int32_t* topk_out, float* alpha_out, float* logits_out,
+                             cudaStream_t stream);
 int launch_rank_average(const uint16_t* qkeys, int P, int E, float* bias_out,
                         cudaStream_t stream);
 int launch_maxvio(const int32_t* topk, int64_t N, int E, int k, int64_t batch_tokens,

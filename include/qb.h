@@ -207,8 +207,17 @@ int lei_inject(float* grad, const int32_t* topk_idx, int64_t N, int E, int k, fl
 int qb_router_gemm(const void* hidden, const void* w_t, int64_t M, int H, int E, float* logits_out,
                    void* stream);
 
-/* Router GEMM followed by the EQB hi pass on its logits (same outputs as
- * qb_route_hist_hi on logits_out, which is required: the hi pass reads it). */
+/* The router GEMM with the EQB hi pass in its epilogue ([QB-PR]
+ * "Implementation": classification and histogram counts added to the router
+ * kernel, no full score tensor kept): the logits stay in tensor memory and
+ * sigmoid, top-(k+1), margins, keys and hi-byte counts are computed there.
+ * Outputs equal qb_route_hist_hi run on this GEMM's fp32 logits (same
+ * binary32 steps): hist_hi += counts; keys_out, topk_out, alpha_out as in
+ * qb_route_hist_hi (each optional); logits_out optional (fp32 [M, E],
+ * written only when given, e.g. to check the outputs).  Arguments as in
+ * qb_router_gemm and qb_route_hist_hi; E = 256, 1 <= k <= 15.  One launch:
+ * a persistent CTA per SM; tokens with more than 8 candidate groups of 8
+ * experts (ties) or a tie at alpha take a slower exact path. */
 int qb_router_gemm_hist_hi(const void* hidden, const void* w_t, int64_t M, int H, int E, int k,
                            const float* bias, float* logits_out, int32_t* hist_hi,
                            uint16_t* keys_out, int32_t* topk_out, float* alpha_out,

@@ -74,3 +74,58 @@ def test_router_gemm_workload(qb, orc):
                topk=topk.cpu().numpy())
     ref = assert_route_matches(orc, res, logits.cpu().numpy(), bias.cpu().numpy(), w.k)
     assert np.array_equal(hist.cpu().numpy(), orc.hist_hi(orc.keys(ref["margins"])))
+
+
+def _fused(qb, hidden, w_t, bias, k, with_logits=True):
+    M = hidden.shape[0]
+    dev = hidden.device
+    logits = torch.empty(M, 256, dtype=torch.float32, device=dev) if with_logits else None
+    hist = torch.zeros(256, 256, dtype=torch.int32, device=dev)
+    keys = torch.empty(M, 256, dtype=torch.int16, device=dev)
+    topk = torch.empty(M, k, dtype=torch.int32, device=dev)
+    alpha = torch.empty(M, dtype=torch.float32, device=dev)
+    qb.qb_router_gemm_hist_hi(hidden, w_t, bias, k, logits, hist, keys_out=keys, topk_out=topk,
+                              alpha_out=alpha)
+    torch.cuda.synchronize()
+    assert qb.device_status() == 0
+    return logits, dict(hist=hist.cpu().numpy(), keys=keys.cpu().numpy().view(np.uint16),
+                        topk=topk.cpu().numpy(), alpha=alpha.cpu().numpy())
+
+
+@pytest.mark.parametrize("M,H,k", [(1000, 128, 6), (300, 2048, 8), (129, 64, 1), (5000, 256, 15)])
+def test_fused_epilogue_matches_routing_of_its_logits(qb, orc, M, H, k):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(M * 7 + H + k)
+    hidden = torch.randn(M, H, generator=g, device="cuda").to(torch.bfloat16)
+    W = (torch.randn(H, 256, generator=g, device="cuda") * H ** -0.5).to(torch.bfloat16)
+    w_t = W.t().contiguous()
+    bias = (torch.rand(256, generator=g, device="cuda") * 2 - 1) * 0.1
+    logits, res = _fused(qb, hidden, w_t, bias, k)
+    # the epilogue's logits are the plain GEMM's, bit for bit (same MMA sequence)
+    plain = torch.empty_like(logits)
+    qb.qb_router_gemm(hidden, w_t, plain)
+    torch.cuda.synchronize()
+    assert torch.equal(logits.view(torch.int32), plain.view(torch.int32))
+    ref = assert_route_matches(orc, res, logits.cpu().numpy(), bias.cpu().numpy(), k)
+    assert np.array_equal(res["hist"], orc.hist_hi(orc.keys(ref["margins"])))
+    # without logits_out the outputs are the same
+    _, res2 = _fused(qb, hidden, w_t, bias, k, with_logits=False)
+    for key in ("hist", "keys", "topk", "alpha"):
+        assert np.array_equal(res2[key], res[key]), key
+
+
+def test_fused_epilogue_exact_path_on_ties(qb, orc):
+    # W's 256 columns repeat 8 distinct ones: every group of 8 experts holds
+    # the same values, so all 32 groups tie at tau (more candidates than the
+    # staging holds) and alpha is tied many times over; bias 0
+    M, H, k = 512, 128, 6
+    g = torch.Generator(device="cuda")
+    g.manual_seed(3)
+    hidden = torch.randn(M, H, generator=g, device="cuda").to(torch.bfloat16)
+    W8 = (torch.randn(H, 8, generator=g, device="cuda") * H ** -0.5).to(torch.bfloat16)
+    W = W8.repeat(1, 32)
+    w_t = W.t().contiguous()
+    bias = torch.zeros(256, dtype=torch.float32, device="cuda")
+    logits, res = _fused(qb, hidden, w_t, bias, k)
+    ref = assert_route_matches(orc, res, logits.cpu().numpy(), bias.cpu().numpy(), k)
+    assert np.array_equal(res["hist"], orc.hist_hi(orc.keys(ref["margins"])))

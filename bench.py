@@ -509,16 +509,37 @@ def main():
         gr_h = fs.grads[0].cpu().pin_memory()
         gr_out = torch.empty_like(gr_h).pin_memory()
         b_out = torch.empty(fs.L, E, dtype=torch.float32).pin_memory()
-        d_lg = torch.empty_like(fs.logits[0])
-        d_gr = torch.empty_like(fs.grads[0])
+        # two device buffer sets; layer l+1's inputs are copied in on one
+        # stream and layer l-1's gradient and bias copied out on another
+        # while layer l computes
+        d_lg = [torch.empty_like(fs.logits[0]) for _ in range(2)]
+        d_gr = [torch.empty_like(fs.grads[0]) for _ in range(2)]
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        comp = torch.cuda.current_stream()
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_done = [torch.cuda.Event() for _ in range(2)]
+        ev_free = [torch.cuda.Event() for _ in range(2)]
 
         def e2e_step():
+            s_in.wait_stream(comp)
+            s_out.wait_stream(comp)
             for l in range(fs.L):
-                d_lg.copy_(lg_h, non_blocking=True)
-                d_gr.copy_(gr_h, non_blocking=True)
-                fs.layer(l, logits=d_lg, grad=d_gr)
-                gr_out.copy_(d_gr, non_blocking=True)
-                b_out[l].copy_(fs.bias[l], non_blocking=True)
+                j = l & 1
+                with torch.cuda.stream(s_in):
+                    if l >= 2:
+                        s_in.wait_event(ev_free[j])
+                    d_lg[j].copy_(lg_h, non_blocking=True)
+                    d_gr[j].copy_(gr_h, non_blocking=True)
+                    ev_in[j].record(s_in)
+                comp.wait_event(ev_in[j])
+                fs.layer(l, logits=d_lg[j], grad=d_gr[j])
+                ev_done[j].record(comp)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_done[j])
+                    gr_out.copy_(d_gr[j], non_blocking=True)
+                    b_out[l].copy_(fs.bias[l], non_blocking=True)
+                    ev_free[j].record(s_out)
+            comp.wait_stream(s_out)  # the step ends with its last copy out
 
         e2e_steps = max(1, min(args.steps, 3))
         ms_e2e = _timed(e2e_step, e2e_steps, 1, dist_on)

@@ -42,8 +42,8 @@ METRIC = "QB routed tokens/s per layer (E=256,k=6, 2-pass EQB) on 1 GB300; % of 
 # launch on a 524288-token layer, from the ncu capture summarised in
 # profiles/route_kernel_hi_one_layer.md.  Reported only while the kernel's
 # sources hash to the value they had when the counters were taken.
-ROUTE_TRAFFIC = {"sha1": "71fb67e8e659547d48334a25097dbb38c4ca1112", "tokens": 524288,
-                 "bytes": (537.019648 + 245.241088) * 1e6}
+ROUTE_TRAFFIC = {"sha1": "b2645c7e52c3878e148156b8476fbf9e83b2f1bd", "tokens": 524288,
+                 "bytes": (537.022464 + 245.423872) * 1e6}
 ROUTE_SOURCES = ("qb_route.cuh", "qb_device.cuh", "qb_route_hi.cu")
 UNIT = "tokens/s/layer"
 WORKLOAD = "full_step"

@@ -246,14 +246,19 @@ __device__ __forceinline__ void issue_rows(unsigned char* tile, const T* logits,
 // Issue the load of every row group of the next tile that is complete inside
 // [0, nf) and not issued yet (groups below `issued`); one mbarrier per group.
 template <int E, typename T, int TILE, int GR>
+// Called by every lane with the same arguments (the bookkeeping stays warp-
+// uniform); only the leader lane issues the barrier arrival and the copy.
 __device__ __forceinline__ void issue_groups(unsigned char* tile, const T* logits, int64_t start,
-                                             int nrows, int nf, int& issued, uint64_t* bars) {
+                                             int nrows, int nf, int& issued, uint64_t* bars,
+                                             bool leader) {
   while (issued * GR < nrows) {
     const int r0 = issued * GR;
     const int r1 = (r0 + GR < nrows) ? r0 + GR : nrows;
     if (nf < r1) break;
-    mbar_arrive_expect_tx(bars + issued, (uint32_t)((r1 - r0) * E * sizeof(T)));
-    issue_rows<E, T, TILE>(tile, logits, start, r0, r1, bars + issued);
+    if (leader) {
+      mbar_arrive_expect_tx(bars + issued, (uint32_t)((r1 - r0) * E * sizeof(T)));
+      issue_rows<E, T, TILE>(tile, logits, start, r0, r1, bars + issued);
+    }
     ++issued;
   }
 }
@@ -375,7 +380,7 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
     const int64_t t0 = tix * TILE;
     const int rows = (int)((a.N - t0) < TILE ? (a.N - t0) : TILE);
     int issued = 0;
-    issue_groups<E, T, TILE, GR>(tile, logits, t0, rows, rows, issued, bars);
+    issue_groups<E, T, TILE, GR>(tile, logits, t0, rows, rows, issued, bars, true);
   }
 
   for (; tix < n_tiles && ok; tix += wstride) {
@@ -736,9 +741,9 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
         }
       }
       __syncwarp();
-      if (lane == 0 && nrows > 0)
+      if (nrows > 0)
         issue_groups<E, T, TILE, GR>(tile, logits, n0, nrows, rows_free<E, T, TILE>((st + 1) * 256),
-                                     issued, bars);
+                                     issued, bars, lane == 0);
     }
   }
 

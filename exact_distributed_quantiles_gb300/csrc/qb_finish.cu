@@ -33,8 +33,11 @@ constexpr int kLoEG = 32;                // experts per CTA slice
 constexpr int kLoRowW = 257;             // words per expert row in shared memory
 constexpr int kLoSmemWords = kLoEG * kLoRowW + 8 * 32;
 
+// No "memory" clobber: nothing reads the counters before the __syncthreads
+// that precedes the flush, and without it the compiler may schedule the
+// next loads ahead of the increments.
 __device__ __forceinline__ void red_shared(uint32_t addr, uint32_t v) {
-  asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+  asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(addr), "r"(v));
 }
 
 __global__ void __launch_bounds__(kLoThreads)

@@ -80,9 +80,22 @@ struct FusedArgs {
   int* status;
 };
 
+// The window slot of a hi byte computed in registers (the same map as the
+// routing kernel's table: bytes 0x40-0x4F -> 0-15, 0xB0-0xBF -> 16-31, any
+// other -> the dummy row 32).  The epilogue has issue slots to spare, and a
+// table load would put shared-memory latency in front of every increment.
+__device__ __forceinline__ uint32_t window_slot(uint32_t bin) {
+  const uint32_t in_window = (0x0810u >> (bin >> 4)) & 1u;  // hi nibble 4 or 11
+  const uint32_t slot = (bin & 15u) | ((bin >> 3) & 16u);
+  return in_window ? slot : (uint32_t)route::kDummy;
+}
+
+// No "memory" clobber: the window is read only after the __syncthreads
+// before the flush, and without the clobber the compiler can issue the
+// loads of a chunk ahead of its increments.
 template <uint32_t V>
 __device__ __forceinline__ void red_shared_addc(uint32_t addr) {
-  asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(addr), "n"(V) : "memory");
+  asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(addr), "n"(V));
 }
 
 template <int KL, int K1>
@@ -401,16 +414,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 4; ++i)
               dst[i] = make_uint4(kw[4 * i], kw[4 * i + 1], kw[4 * i + 2], kw[4 * i + 3]);
           }
+          // every element is counted in the window without branching; a bin
+          // outside it lands in the dummy row (never flushed) and is counted
+          // again below, in global memory, by the rare second loop
+          uint32_t mslot = 0;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const uint32_t bin = prmt(kw[i >> 1], 0u, (i & 1) ? 0x4443u : 0x4441u);
-            const uint32_t slot = lut[bin];
-            if (slot == (uint32_t)route::kDummy)
-              atomicAdd(g.hist + (int64_t)(32 * c + i) * 256 + bin, 1);
-            else if (i & 1)
-              red_shared_addc<0x10000u>(win_b + 4u * (slot * (uint32_t)kWinRow + 16u * c + (i >> 1)));
+            const uint32_t slot = window_slot(bin);
+            mslot = slot > mslot ? slot : mslot;
+            const uint32_t addr = win_b + 4u * (slot * (uint32_t)kWinRow + 16u * c + (i >> 1));
+            if (i & 1)
+              red_shared_addc<0x10000u>(addr);
             else
-              red_shared_addc<1u>(win_b + 4u * (slot * (uint32_t)kWinRow + 16u * c + (i >> 1)));
+              red_shared_addc<1u>(addr);
+          }
+          if (mslot == (uint32_t)route::kDummy) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const uint32_t bin = prmt(kw[i >> 1], 0u, (i & 1) ? 0x4443u : 0x4441u);
+              if (lut[bin] == (uint32_t)route::kDummy)
+                atomicAdd(g.hist + (int64_t)(32 * c + i) * 256 + bin, 1);
+            }
           }
         }
       };

@@ -34,8 +34,9 @@ namespace {
 constexpr int kCountThreads = 1024;
 constexpr int kCountSmemMax = 200 * 1024;
 
+// No "memory" clobber: the counters are read only after a __syncthreads.
 __device__ __forceinline__ void red_shared_u32(uint32_t addr, uint32_t v) {
-  asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+  asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(addr), "r"(v));
 }
 
 // EG experts per CTA (8 or 16): EG / 8 lanes per row, each lane reads 8

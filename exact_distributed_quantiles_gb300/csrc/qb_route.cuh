@@ -305,8 +305,11 @@ __device__ __forceinline__ void keys8(float alpha, const float (&s)[8], uint32_t
 }
 
 
+// No "memory" clobber: the window is read only after the __syncthreads
+// before the flush, and without the clobber the compiler can issue a step's
+// table loads ahead of its increments.
 __device__ __forceinline__ void red_shared_add1(uint32_t addr) {
-  asm volatile("red.shared.add.u32 [%0], 1;" ::"r"(addr) : "memory");
+  asm volatile("red.shared.add.u32 [%0], 1;" ::"r"(addr));
 }
 
 __device__ __forceinline__ uint32_t lut_load(const uint8_t* lut, uint32_t bin) {

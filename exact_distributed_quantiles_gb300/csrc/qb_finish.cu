@@ -23,21 +23,22 @@ namespace {
 // per-SM histograms through L2 atomics would cost more than the pass itself).
 // Four lanes cover one row slice (16 bytes = 8 keys each), a warp covers 8
 // rows per load; loads are double-buffered in registers.  Every key issues one
-// shared atomic: a key whose hi byte is not the selected one goes to a
-// per-lane dummy slot that is never flushed, so lanes never branch on their
-// own matches.  Layout: counter (e, lo) at word e * 257 + lo (257 spreads the
-// experts over the banks); dummies at 32 * 257 + j * 32 + lane.
+// shared increment without branching: with t = key ^ (sel << 8) the low byte
+// is the key's, the high byte zero exactly when the key is in the selected
+// bin, so min(t, 256) is the counter's index, or 256 -- the 257th word of the
+// expert's row, never flushed -- for every other key.  Layout: counter
+// (e, lo) at word e * 257 + lo (257 spreads the experts over the banks).
 // ------------------------------------------------------------------------
 constexpr int kLoThreads = 256;
 constexpr int kLoEG = 32;                // experts per CTA slice
 constexpr int kLoRowW = 257;             // words per expert row in shared memory
-constexpr int kLoSmemWords = kLoEG * kLoRowW + 8 * 32;
+constexpr int kLoSmemWords = kLoEG * kLoRowW;
 
 // No "memory" clobber: nothing reads the counters before the __syncthreads
 // that precedes the flush, and without it the compiler may schedule the
 // next loads ahead of the increments.
-__device__ __forceinline__ void red_shared(uint32_t addr, uint32_t v) {
-  asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(addr), "r"(v));
+__device__ __forceinline__ void red_shared1(uint32_t addr) {
+  asm volatile("red.shared.add.u32 [%0], 1;" ::"r"(addr));
 }
 
 __global__ void __launch_bounds__(kLoThreads)
@@ -64,12 +65,9 @@ __global__ void __launch_bounds__(kLoThreads)
     spat[i] = ((uint32_t)(sel[eg * kLoEG + el0 + 2 * i] & 0xFF) << 8) |
               ((uint32_t)(sel[eg * kLoEG + el0 + 2 * i + 1] & 0xFF) << 24);
   const uint32_t hb = (uint32_t)__cvta_generic_to_shared(h);
-  uint32_t ebase[8], dummy[8];
+  uint32_t ebase[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    ebase[j] = hb + 4u * (uint32_t)((el0 + j) * kLoRowW);
-    dummy[j] = hb + 4u * (uint32_t)(kLoEG * kLoRowW + j * 32 + lane);
-  }
+  for (int j = 0; j < 8; ++j) ebase[j] = hb + 4u * (uint32_t)((el0 + j) * kLoRowW);
   __syncthreads();
 
   const int64_t n_rows = r_end > r_begin ? r_end - r_begin : 0;
@@ -99,10 +97,8 @@ __global__ void __launch_bounds__(kLoThreads)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const uint32_t x = w[i] ^ spat[i];  // selected hi bytes become 0
-          const uint32_t a0 = ebase[2 * i] + 4u * (w[i] & 0xFFu);
-          const uint32_t a1 = ebase[2 * i + 1] + 4u * ((w[i] >> 16) & 0xFFu);
-          red_shared((x & 0x0000FF00u) ? dummy[2 * i] : a0, 1u);
-          red_shared((x & 0xFF000000u) ? dummy[2 * i + 1] : a1, 1u);
+          red_shared1(ebase[2 * i] + 4u * min(x & 0xFFFFu, 256u));
+          red_shared1(ebase[2 * i + 1] + 4u * min(x >> 16, 256u));
         }
       }
       cur[q] = nxt[q];

@@ -45,8 +45,31 @@ METRIC = "QB routed tokens/s per layer (E=256,k=6, 2-pass EQB) on 1 GB300; % of 
 ROUTE_TRAFFIC = {"sha1": "b2645c7e52c3878e148156b8476fbf9e83b2f1bd", "tokens": 524288,
                  "bytes": (537.022464 + 245.423872) * 1e6}
 ROUTE_SOURCES = ("qb_route.cuh", "qb_device.cuh", "qb_route_hi.cu")
+# Warp instructions of the same capture (smsp__inst_executed.sum), for the
+# issue-rate roofline of this issue-bound kernel; same hash guard.
+ROUTE_INSTR = {"tokens": 524288, "warp_instructions": None}
 UNIT = "tokens/s/layer"
 WORKLOAD = "full_step"
+
+
+def _route_sources_match() -> bool:
+    import hashlib
+    h = hashlib.sha1()
+    for f in ROUTE_SOURCES:
+        with open(os.path.join(ROOT, "exact_distributed_quantiles_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest() == ROUTE_TRAFFIC["sha1"]
+
+
+def _issue_peak():
+    """Warp-instruction issue peak: SMs x 4 schedulers x 1 instruction per
+    cycle x the maximum SM clock (MEASURED_PEAKS.json's, else 2070 MHz)."""
+    try:
+        mhz = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["sm_max_mhz"])
+    except Exception:
+        mhz = 2070.0
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return sms * 4 * mhz * 1e6
 
 
 def _route_traffic(tokens: int):
@@ -610,6 +633,13 @@ def main():
                          "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                          "unit": "GB/s", "frac": achieved / peak, "traffic": _route_traffic(n),
                          "bytes_per_launch": hi_bytes, "avg_launch_ms": hi_avg_ms},
+            "roofline_issue": (None if ROUTE_INSTR["warp_instructions"] is None
+                               or not _route_sources_match() else {
+                "bound": "alu", "kernel": "qb_route_hist_hi (route_kernel hi mode)",
+                "achieved": ROUTE_INSTR["warp_instructions"] * n / ROUTE_INSTR["tokens"]
+                / (hi_avg_ms / 1e3), "peak": _issue_peak(), "unit": "warp instructions/s",
+                "frac": ROUTE_INSTR["warp_instructions"] * n / ROUTE_INSTR["tokens"]
+                / (hi_avg_ms / 1e3) / _issue_peak()}),
             "cpu_baseline": cpu,
             "e2e": e2e,
             "components": comps,

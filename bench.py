@@ -166,59 +166,78 @@ class FullStep:
         self.hist_lo = torch.zeros(layers, E, 256, dtype=torch.int32, device=dev)
         self.sel = torch.zeros(layers, E, dtype=torch.int32, device=dev)
         self.r_lo = torch.zeros(layers, E, dtype=torch.int32, device=dev)
-        # keys, top-k sets and LEI workspace alternate between layers, so that a
-        # layer's LEI (on a second stream) can run beside the next layer's EQB
-        self.keys = [torch.empty(n, E, dtype=torch.int16, device=dev) for _ in range(2)]
+        # top-k sets and LEI workspaces alternate between layers: a layer's
+        # LEI finishes while the next layer routes
+        self.keys = torch.empty(n, E, dtype=torch.int16, device=dev)
         self.topk = [torch.empty(n, k, dtype=torch.int32, device=dev) for _ in range(2)]
         self.ws = [torch.empty(w.n_micro, E, dtype=torch.float32, device=dev) for _ in range(2)]
         self.side = torch.cuda.Stream(device=dev)
         self.ev_hi = [torch.cuda.Event() for _ in range(2)]
-        self.ev_lei = [torch.cuda.Event() for _ in range(2)]
+        self.ev_rho = [torch.cuda.Event() for _ in range(2)]
+        self.pending = None  # (grad, slot) of a layer whose grad update is still to be enqueued
         self.R = qb.rank(n, E, k)
         self.launches_per_layer = {"eqb": 5, "lei": 2}
         self.hi_events = []
 
     def layer(self, l, logits=None, grad=None, lei=True, time_hi=False, join=False):
-        """One layer: EQB on the current stream; LEI (it needs only this
-        layer's top-k sets) on the second stream, beside the EQB tail and the
-        next layer.  join=True makes the current stream wait for the LEI."""
+        """One layer.  EQB runs on the current stream.  LEI needs only this
+        layer's top-k sets: its rho kernel runs on a second stream beside the
+        EQB tail, and its grad update is enqueued right behind the NEXT
+        layer's hi pass as a programmatic dependent (lei_apply_overlap), so
+        that the bulk-copy unit streams the gradient while that pass routes.
+        join=True (or flush()) enqueues the pending grad update at once."""
         qb, w = self.qb, self.w
         j = l & 1
         main = torch.cuda.current_stream()
         lg = self.logits[l] if logits is None else logits
-        if l >= 2 or join:
-            main.wait_event(self.ev_lei[j])  # the LEI that last read topk[j] is done
+        prev = self.pending
+        if prev is not None:
+            main.wait_event(self.ev_rho[prev[1]])  # its eta*rho is in the workspace
         if time_hi:
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record()
-        qb.qb_route_hist_hi(lg, self.bias[l], w.k, self.hist_hi[l], keys_out=self.keys[j],
+        qb.qb_route_hist_hi(lg, self.bias[l], w.k, self.hist_hi[l], keys_out=self.keys,
                             topk_out=self.topk[j])
         if time_hi:
             e1.record()
             self.hi_events.append((e0, e1))
+        if prev is not None:
+            if time_hi:  # (not behind the timed pass)
+                qb.lei_apply(prev[0], self.ws[prev[1]], batch_tokens=w.n_tokens)
+            else:
+                qb.lei_apply_overlap(prev[0], self.ws[prev[1]], batch_tokens=w.n_tokens)
+            self.pending = None
         self.ev_hi[j].record(main)
         if lei:
-            g = self.grads[l] if grad is None else grad
             self.side.wait_event(self.ev_hi[j])
             with torch.cuda.stream(self.side):
-                qb.lei_inject(g, self.topk[j], w.eta, self.ws[j], batch_tokens=w.n_tokens)
-            self.ev_lei[j].record(self.side)
+                qb.lei_rho(self.topk[j], w.E, w.eta, self.ws[j], batch_tokens=w.n_tokens)
+            self.ev_rho[j].record(self.side)
+            self.pending = (self.grads[l] if grad is None else grad, j)
         qb.qb_select_hi(self.hist_hi[l], self.R, self.sel[l], self.r_lo[l])
-        qb.qb_keys_hist_lo(self.keys[j], self.sel[l], self.hist_lo[l])
+        qb.qb_keys_hist_lo(self.keys, self.sel[l], self.hist_lo[l])
         qb.qb_finalize(self.hist_hi[l], self.hist_lo[l], self.sel[l], self.r_lo[l], self.bias[l],
                        reset=True)
-        if join and lei:
-            main.wait_event(self.ev_lei[j])
+        if join:
+            self.flush()
+
+    def flush(self):
+        """Enqueue the pending grad update (the last layer's) on the current stream."""
+        if self.pending is not None:
+            g, j = self.pending
+            main = torch.cuda.current_stream()
+            main.wait_event(self.ev_rho[j])
+            self.qb.lei_apply(g, self.ws[j], batch_tokens=self.w.n_tokens)
+            self.pending = None
 
     def step(self, lei=True, time_hi=False):
         main = torch.cuda.current_stream()
         self.side.wait_stream(main)
-        for e in self.ev_lei:
-            e.record(main)  # nothing outstanding from an earlier step
         for l in range(self.L):
             self.layer(l, lei=lei, time_hi=time_hi)
-        main.wait_stream(self.side)  # the step ends with its last LEI
+        self.flush()
+        main.wait_stream(self.side)
 
 
 def _timed(fn, steps, warmup, dist_on):
@@ -591,8 +610,7 @@ def main():
         def e2e_step():
             s_in.wait_stream(comp)
             s_out.wait_stream(comp)
-            for e in fs.ev_lei:  # (last recorded inside the graph capture)
-                e.record(comp)
+            fs.side.wait_stream(comp)
             for l in range(fs.L):
                 j = l & 1
                 with torch.cuda.stream(s_in):

@@ -200,6 +200,45 @@ int lei_inject(float* grad, const int32_t* topk_idx, int64_t N, int E, int k, fl
   return launch_lei(grad, topk_idx, N, E, k, eta, batch_tokens, workspace, as_stream(stream));
 }
 
+int lei_rho(const int32_t* topk_idx, int64_t N, int E, int k, float eta, int64_t batch_tokens,
+            float* workspace, void* stream) {
+  if (!topk_idx || !workspace) return QB_EINVAL;
+  if (!aligned16(workspace)) return QB_EINVAL;
+  if (N < 0 || batch_tokens < 0) return QB_EINVAL;
+  if (!supported_E(E)) return QB_EUNSUPPORTED;
+  if (k < 1 || k >= E) return QB_EINVAL;
+  if (N == 0) return QB_OK;
+  if (batch_tokens == 0 || batch_tokens > N) batch_tokens = N;
+  if (N > INT32_MAX) return QB_EOVERFLOW;
+  const int64_t nb = (N + batch_tokens - 1) / batch_tokens;
+  if (nb > INT32_MAX) return QB_EINVAL;
+  return launch_lei_rho(topk_idx, N, E, k, eta, batch_tokens, workspace, as_stream(stream));
+}
+
+int lei_apply(float* grad, int64_t N, int E, int64_t batch_tokens, const float* workspace,
+              void* stream) {
+  if (!grad || !workspace) return QB_EINVAL;
+  if (!aligned16(grad) || !aligned16(workspace)) return QB_EINVAL;
+  if (N < 0 || batch_tokens < 0) return QB_EINVAL;
+  if (!supported_E(E)) return QB_EUNSUPPORTED;
+  if (N == 0) return QB_OK;
+  if (batch_tokens == 0 || batch_tokens > N) batch_tokens = N;
+  if (N > INT32_MAX) return QB_EOVERFLOW;
+  return launch_lei_apply(grad, N, E, batch_tokens, workspace, as_stream(stream));
+}
+
+int lei_apply_overlap(float* grad, int64_t N, int E, int64_t batch_tokens, const float* workspace,
+                      void* stream) {
+  if (!grad || !workspace) return QB_EINVAL;
+  if (!aligned16(grad) || !aligned16(workspace)) return QB_EINVAL;
+  if (N < 0 || batch_tokens < 0) return QB_EINVAL;
+  if (!supported_E(E)) return QB_EUNSUPPORTED;
+  if (N == 0) return QB_OK;
+  if (batch_tokens == 0 || batch_tokens > N) batch_tokens = N;
+  if (N > INT32_MAX) return QB_EOVERFLOW;
+  return launch_lei_apply_overlap(grad, N, E, batch_tokens, workspace, as_stream(stream));
+}
+
 int qb_router_gemm(const void* hidden, const void* w_t, int64_t M, int H, int E, float* logits_out,
                    void* stream) {
   if (!hidden || !w_t || !logits_out) return QB_EINVAL;

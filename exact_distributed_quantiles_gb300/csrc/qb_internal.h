@@ -56,6 +56,12 @@ int launch_maxvio(const int32_t* topk, int64_t N, int E, int k, int64_t batch_to
 int launch_sigmoid(const float* x, float* s, int64_t n, cudaStream_t stream);
 int launch_lei(float* grad, const int32_t* topk, int64_t N, int E, int k, float eta,
                int64_t batch_tokens, float* workspace, cudaStream_t stream);
+int launch_lei_rho(const int32_t* topk, int64_t N, int E, int k, float eta,
+                   int64_t batch_tokens, float* workspace, cudaStream_t stream);
+int launch_lei_apply(float* grad, int64_t N, int E, int64_t batch_tokens, const float* workspace,
+                     cudaStream_t stream);
+int launch_lei_apply_overlap(float* grad, int64_t N, int E, int64_t batch_tokens,
+                             const float* workspace, cudaStream_t stream);
 
 int launch_router_gemm(const void* hidden, const void* w_t, int64_t M, int K, int E,
                        float* logits, cudaStream_t stream);

@@ -214,49 +214,108 @@ __global__ void __launch_bounds__(kMaxvioThreads) maxvio_kernel(
   }
 }
 
-// grad += c[batch(row)] streamed in 16-byte chunks.  Each CTA walks whole
-// rows (32-bit row arithmetic, one division per row), four chunks in flight
-// per thread.
-constexpr int kApplyThreads = 256;
+// grad += c[batch(row)] streamed in 16-byte chunks.  Each CTA owns a fixed
+// run of kApplyIters blocks of rows; in a block every thread has kApplyU
+// loads in flight.  The CTAs are small (128 threads, at most 72 registers)
+// so that one fits on an SM beside a resident routing CTA, and the grid
+// drains through whatever room the other kernels of the step leave.
+constexpr int kApplyThreads = 128;
+constexpr int kApplyU = 8;
+constexpr int kApplyIters = 4;
 
-__global__ void __launch_bounds__(kApplyThreads) lei_apply_kernel(float* __restrict__ grad,
-                                                                  int N, int e4_log2,
-                                                                  int batch_tokens,
-                                                                  const float* __restrict__ ws) {
-  const int e4 = 1 << e4_log2;                 // 16-byte chunks per row
-  const int rows_per_pass = kApplyThreads >> e4_log2 ? kApplyThreads >> e4_log2 : 1;
-  const int lanes_per_row = kApplyThreads < e4 ? kApplyThreads : e4;
-  const int r_in = threadIdx.x >> (e4_log2 < 8 ? e4_log2 : 8);
+__global__ void __launch_bounds__(kApplyThreads, 7)
+    lei_apply_kernel(float* __restrict__ grad, int N, int e4_log2, int batch_tokens,
+                     const float* __restrict__ ws) {
+  const int e4 = 1 << e4_log2;  // 16-byte chunks per row
+  const int lanes_log2 = e4_log2 < 7 ? e4_log2 : 7;  // lanes per row: min(e4, 128)
+  const int lanes_per_row = 1 << lanes_log2;
+  const int rows_per_pass = kApplyThreads >> lanes_log2;
+  const int r_in = threadIdx.x >> lanes_log2;
   const int c_in = threadIdx.x & (lanes_per_row - 1);
+  const int block_rows = rows_per_pass * kApplyU;
   float4* g4 = reinterpret_cast<float4*>(grad);
   const float4* c4 = reinterpret_cast<const float4*>(ws);
-  constexpr int kU = 4;
-  const int64_t stride = (int64_t)gridDim.x * rows_per_pass * kU;
-  for (int64_t r0 = (int64_t)blockIdx.x * rows_per_pass * kU; r0 < N; r0 += stride) {
+  int64_t rb = (int64_t)blockIdx.x * block_rows * kApplyIters;
+  for (int it = 0; it < kApplyIters && rb < N; ++it, rb += block_rows) {
+    const int r0 = (int)rb;
+    const int last = (int)(rb + block_rows < N ? rb + block_rows : N) - 1;
+    const int b0 = r0 / batch_tokens;
+    const bool one_batch = last / batch_tokens == b0;  // almost always
     for (int col = c_in; col < e4; col += lanes_per_row) {
-      float4 g[kU], c[kU];
-      int rr[kU];
+      float4 g[kApplyU];
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        rr[u] = (int)(r0 + u * rows_per_pass + r_in);
-        if (rr[u] < N) {
-          g[u] = __ldcs(g4 + ((int64_t)rr[u] << e4_log2) + col);
-          c[u] = __ldg(c4 + ((int64_t)(rr[u] / batch_tokens) << e4_log2) + col);
-        }
+      for (int u = 0; u < kApplyU; ++u) {
+        const int rr = r0 + u * rows_per_pass + r_in;
+        if (rr <= last) g[u] = __ldcs(g4 + ((int64_t)rr << e4_log2) + col);
       }
+      float4 c = __ldg(c4 + ((int64_t)b0 << e4_log2) + col);
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        if (rr[u] < N) {
+      for (int u = 0; u < kApplyU; ++u) {
+        const int rr = r0 + u * rows_per_pass + r_in;
+        if (rr <= last) {
+          if (!one_batch) c = __ldg(c4 + ((int64_t)(rr / batch_tokens) << e4_log2) + col);
           float4 o;
-          o.x = __fadd_rn(g[u].x, c[u].x);
-          o.y = __fadd_rn(g[u].y, c[u].y);
-          o.z = __fadd_rn(g[u].z, c[u].z);
-          o.w = __fadd_rn(g[u].w, c[u].w);
-          __stcs(g4 + ((int64_t)rr[u] << e4_log2) + col, o);
+          o.x = __fadd_rn(g[u].x, c.x);
+          o.y = __fadd_rn(g[u].y, c.y);
+          o.z = __fadd_rn(g[u].z, c.z);
+          o.w = __fadd_rn(g[u].w, c.w);
+          __stcs(g4 + ((int64_t)rr << e4_log2) + col, o);
         }
       }
     }
   }
+}
+
+// The same update done by the bulk-copy unit: a cp.reduce.async.bulk .add.f32
+// from a 4 KB shared block holding the batch's c repeated over `rep` rows adds
+// c to `rep` rows of grad in L2 per instruction.  No registers or SM load /
+// store bandwidth are spent on grad, and a CTA (one warp, 4 KB of shared
+// memory) fits beside a resident routing CTA.  One CTA per SM, each over an
+// even share of the row groups; the last step waits for the kernel this one
+// was launched behind (a no-op without a programmatic launch), so that its
+// completion implies that kernel's.
+constexpr int kBulkBytes = 4096;
+
+__global__ void __launch_bounds__(32) lei_apply_bulk_kernel(float* __restrict__ grad, int N, int E,
+                                                            int batch_tokens,
+                                                            const float* __restrict__ ws) {
+  __shared__ __align__(128) float buf[kBulkBytes / 4];
+  const int lane = threadIdx.x;
+  const int rep = kBulkBytes / (E * 4);  // rows per bulk op (E <= 512: at least 2)
+  const int e4 = E >> 2;
+  const int64_t groups = ((int64_t)N + rep - 1) / rep;
+  const int64_t g0 = groups * blockIdx.x / gridDim.x;
+  const int64_t g1 = groups * (blockIdx.x + 1) / gridDim.x;
+  int64_t r = g0 * rep;
+  const int64_t r_end = g1 * rep < N ? g1 * rep : N;
+  const uint32_t src = (uint32_t)__cvta_generic_to_shared(buf);
+  while (r < r_end) {
+    const int64_t b = r / batch_tokens;
+    const int64_t seg_end = (b + 1) * batch_tokens < r_end ? (b + 1) * batch_tokens : r_end;
+    // refill only after the ops issued from the old contents have read them
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    __syncwarp();
+    const float4* c4 = reinterpret_cast<const float4*>(ws + b * E);
+    float4* b4 = reinterpret_cast<float4*>(buf);
+    for (int i = lane; i < kBulkBytes / 16; i += 32) b4[i] = __ldg(c4 + (i & (e4 - 1)));
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+      for (int64_t q = r; q < seg_end; q += rep) {
+        const int64_t nr = seg_end - q < rep ? seg_end - q : rep;
+        asm volatile(
+            "cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
+                grad + q * E),
+            "r"(src), "r"((uint32_t)(nr * E * 4))
+            : "memory");
+      }
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+    r = seg_end;
+  }
+  if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  __syncwarp();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace
@@ -273,24 +332,56 @@ int launch_maxvio(const int32_t* topk, int64_t N, int E, int k, int64_t batch_to
   return launch_status();
 }
 
-int launch_lei(float* grad, const int32_t* topk, int64_t N, int E, int k, float eta,
-               int64_t batch_tokens, float* workspace, cudaStream_t stream) {
+int launch_lei_rho(const int32_t* topk, int64_t N, int E, int k, float eta,
+                   int64_t batch_tokens, float* workspace, cudaStream_t stream) {
   const int64_t nb = (N + batch_tokens - 1) / batch_tokens;
   const int smem = kRhoWarps * E * (int)sizeof(int32_t);
   lei_rho_kernel<<<(unsigned)(nb * kRhoCluster), kRhoThreads, smem, stream>>>(
       topk, N, E, k, eta, batch_tokens, workspace);
-  int st = launch_status();
-  if (st != QB_OK) return st;
+  return launch_status();
+}
+
+int launch_lei_apply(float* grad, int64_t N, int E, int64_t batch_tokens, const float* workspace,
+                     cudaStream_t stream) {
   int e4_log2 = 0;
   while ((1 << e4_log2) < E / 4) ++e4_log2;  // E is a power of two
-  const int rows_per_pass = (kApplyThreads >> e4_log2) ? (kApplyThreads >> e4_log2) : 1;
-  int64_t grid = (N + rows_per_pass * 4 - 1) / (rows_per_pass * 4);
-  const int64_t gmax = (int64_t)sm_count() * 8;
-  if (grid > gmax) grid = gmax;
-  if (grid < 1) grid = 1;
+  const int lanes_log2 = e4_log2 < 7 ? e4_log2 : 7;
+  const int64_t cta_rows = (int64_t)(kApplyThreads >> lanes_log2) * kApplyU * kApplyIters;
+  const int64_t grid = (N + cta_rows - 1) / cta_rows;
   lei_apply_kernel<<<(unsigned)grid, kApplyThreads, 0, stream>>>(grad, (int)N, e4_log2,
                                                                 (int)batch_tokens, workspace);
   return launch_status();
+}
+
+int launch_lei_apply_overlap(float* grad, int64_t N, int E, int64_t batch_tokens,
+                             const float* workspace, cudaStream_t stream) {
+  const int64_t groups = (N + kBulkBytes / (E * 4) - 1) / (kBulkBytes / (E * 4));
+  int64_t grid = sm_count();
+  if (grid > groups) grid = groups;
+  if (grid < 1) grid = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, lei_apply_bulk_kernel, grad, (int)N, E, (int)batch_tokens,
+                         workspace) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return QB_ECUDA;
+  }
+  return launch_status();
+}
+
+int launch_lei(float* grad, const int32_t* topk, int64_t N, int E, int k, float eta,
+               int64_t batch_tokens, float* workspace, cudaStream_t stream) {
+  const int st = launch_lei_rho(topk, N, E, k, eta, batch_tokens, workspace, stream);
+  if (st != QB_OK) return st;
+  return launch_lei_apply(grad, N, E, batch_tokens, workspace, stream);
 }
 
 }  // namespace qb

@@ -330,6 +330,9 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
   // per-tile branches below need no divergence handling
   const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
   const int lane = threadIdx.x & 31;
+  // A kernel launched as this one's programmatic dependent (lei_apply_overlap)
+  // may be scheduled into the room left beside this CTA from now on.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   unsigned char* wbase = smem + SM::kHist + warp * SM::kWarp;
   unsigned char* tile = wbase;
   float* sc = reinterpret_cast<float*>(tile);

@@ -23,7 +23,8 @@ EXPORTS = ("qb_status_string", "qb_version", "qb_rank", "qb_sigmoid", "qb_zero_i
            "qb_route_hist_hi", "qb_select_hi", "qb_keys_hist_lo", "qb_route_hist_lo",
            "qb_finalize", "k3_route_hist", "k3_finalize", "lei_inject", "qb_device_status",
            "lei_inject_noalloc", "qb_router_gemm", "qb_router_gemm_hist_hi", "qb_rank_average",
-           "qb_maxvio")
+           "qb_maxvio", "lei_rho", "lei_apply",
+           "lei_apply_overlap")
 
 
 class QBError(RuntimeError):
@@ -58,6 +59,9 @@ def _load():
         "qb_router_gemm_hist_hi": (I, [P, P, I64, I, I, I, P, P, P, P, P, P, P]),
         "qb_rank_average": (I, [P, I, I, P, P]),
         "qb_maxvio": (I, [P, I64, I, I, I64, P, P, P]),
+        "lei_rho": (I, [P, I64, I, I, F, I64, P, P]),
+        "lei_apply": (I, [P, I64, I, I64, P, P]),
+        "lei_apply_overlap": (I, [P, I64, I, I64, P, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -176,6 +180,29 @@ def lei_inject(grad, topk_idx, eta, workspace, batch_tokens=0, stream=None):
     _check("lei_inject",
            lib.lei_inject(_ptr(grad), _ptr(topk_idx), N, E, int(k), float(eta), int(batch_tokens),
                           _ptr(workspace), _stream(stream)))
+
+
+def lei_rho(topk_idx, E, eta, workspace, batch_tokens=0, stream=None):
+    """First half of lei_inject: eta*rho per local batch into workspace."""
+    N, k = topk_idx.shape
+    _check("lei_rho", lib.lei_rho(_ptr(topk_idx), N, int(E), int(k), float(eta),
+                                  int(batch_tokens), _ptr(workspace), _stream(stream)))
+
+
+def lei_apply(grad, workspace, batch_tokens=0, stream=None):
+    """Second half of lei_inject: grad += workspace[batch(row)]."""
+    N, E = grad.shape
+    _check("lei_apply", lib.lei_apply(_ptr(grad), N, E, int(batch_tokens), _ptr(workspace),
+                                      _stream(stream)))
+
+
+def lei_apply_overlap(grad, workspace, batch_tokens=0, stream=None):
+    """lei_apply launched to run beside the kernel enqueued just before it
+    on the stream (it must not touch grad or write workspace)."""
+    N, E = grad.shape
+    _check("lei_apply_overlap",
+           lib.lei_apply_overlap(_ptr(grad), N, E, int(batch_tokens), _ptr(workspace),
+                                 _stream(stream)))
 
 
 def lei_inject_noalloc(grad, topk_idx, eta, batch_tokens=0, stream=None):

@@ -191,6 +191,38 @@ int k3_finalize(int32_t* hist, int E, int nbins, int64_t r, float* bounds, float
 int lei_inject(float* grad, const int32_t* topk_idx, int64_t N, int E, int k, float eta,
                int64_t batch_tokens, float* workspace, void* stream);
 
+/* lei_inject in two calls, for schedules that run the two halves at
+ * different times (e.g. the grad update beside the next layer's routing).
+ * lei_rho(...) + lei_apply(...) on one stream with the same workspace give
+ * exactly the result of lei_inject(...).
+ * lei_rho: the per-batch loads and eta*rho of lei_inject written to
+ *   `workspace` (fp32 [num_batches * E], 16-byte aligned, caller-owned);
+ *   grad is not touched.  Arguments and errors as in lei_inject.
+ * lei_apply: grad[i,e] = RN32(grad[i,e] + workspace[batch(i) * E + e]) for
+ *   every token i, batch(i) = i / batch_tokens (0 means one batch of N);
+ *   grad and workspace 16-byte aligned.  The grad update is one launch of
+ *   small CTAs (128 threads), so that it fits beside other resident kernels. */
+int lei_rho(const int32_t* topk_idx, int64_t N, int E, int k, float eta, int64_t batch_tokens,
+            float* workspace, void* stream);
+int lei_apply(float* grad, int64_t N, int E, int64_t batch_tokens, const float* workspace,
+              void* stream);
+
+/* lei_apply launched to run beside the kernel enqueued just before it on
+ * `stream` (a programmatic dependent launch): it may start as soon as every
+ * CTA of that kernel has started (qb_route_hist_hi, qb_route_hist_lo and
+ * k3_route_hist signal this at their start; any other kernel at its exit)
+ * and it completes only after that kernel has completed, so work enqueued
+ * after it sees both.  Use it to overlap the grad stream of one layer with
+ * the routing pass of the next.  Same arguments and result as lei_apply,
+ * bit for bit.  The adds are done by the bulk-copy unit
+ * (cp.reduce.async.bulk .add.f32 into L2, binary32 round-to-nearest-even),
+ * one 32-thread CTA with 4 KB of shared memory per SM.  The caller must
+ * make sure that the preceding kernel neither reads nor writes grad and
+ * does not write workspace (it runs concurrently), and that workspace was
+ * complete before that kernel was enqueued. */
+int lei_apply_overlap(float* grad, int64_t N, int E, int64_t batch_tokens, const float* workspace,
+                      void* stream);
+
 /* --------------------------------------------------------- router GEMM ---- */
 
 /* Router logits on the tensor cores: logits[M, E] = hidden[M, H] x W[H, E],

@@ -103,6 +103,21 @@ def test_argument_errors_are_reported_before_launch(lib):
     assert L.lei_inject(fake, fake, 10, 256, 6, 8e-5, 0, N0, N0) == lib.QB_EINVAL
     assert L.lei_inject(fake, fake, 10, 256, 0, 8e-5, 0, fake, N0) == lib.QB_EINVAL
     assert L.lei_inject(fake, fake, 0, 256, 6, 8e-5, 0, fake, N0) == lib.QB_OK
+    assert L.lei_rho(fake, 10, 256, 6, 8e-5, 0, N0, N0) == lib.QB_EINVAL
+    assert L.lei_rho(fake, 10, 256, 6, 8e-5, 0, odd, N0) == lib.QB_EINVAL
+    assert L.lei_rho(fake, 10, 100, 6, 8e-5, 0, fake, N0) == lib.QB_EUNSUPPORTED
+    assert L.lei_rho(fake, 10, 256, 0, 8e-5, 0, fake, N0) == lib.QB_EINVAL
+    assert L.lei_rho(fake, 0, 256, 6, 8e-5, 0, fake, N0) == lib.QB_OK
+    assert L.lei_apply(odd, 10, 256, 0, fake, N0) == lib.QB_EINVAL
+    assert L.lei_apply(fake, 10, 256, 0, odd, N0) == lib.QB_EINVAL
+    assert L.lei_apply(fake, -1, 256, 0, fake, N0) == lib.QB_EINVAL
+    assert L.lei_apply(fake, 10, 100, 0, fake, N0) == lib.QB_EUNSUPPORTED
+    assert L.lei_apply(fake, 0, 256, 0, fake, N0) == lib.QB_OK
+    assert L.lei_apply_overlap(odd, 10, 256, 0, fake, N0) == lib.QB_EINVAL
+    assert L.lei_apply_overlap(fake, 10, 256, 0, N0, N0) == lib.QB_EINVAL
+    assert L.lei_apply_overlap(fake, 10, 256, -1, fake, N0) == lib.QB_EINVAL
+    assert L.lei_apply_overlap(fake, 10, 48, 0, fake, N0) == lib.QB_EUNSUPPORTED
+    assert L.lei_apply_overlap(fake, 0, 256, 0, fake, N0) == lib.QB_OK
     # rank average and MaxVio
     assert L.qb_rank_average(N0, 2, 256, fake, N0) == lib.QB_EINVAL
     assert L.qb_rank_average(fake, 0, 256, fake, N0) == lib.QB_EINVAL

@@ -1,9 +1,11 @@
 """The benchmark's step schedule computes what the serial layer sequence does.
 
-bench.py runs each layer's LEI on a second stream beside the EQB tail and the
-next layer, with alternating buffers, and replays the whole step from a CUDA
-graph.  Here a 3-layer step run that way must leave every bias and every
-gradient bit-identical to the same layers run one after the other.
+bench.py runs each layer's LEI rho kernel on a second stream beside the EQB
+tail, and enqueues its grad update behind the next layer's hi pass as a
+programmatic dependent launch (lei_apply_overlap, run concurrently with that
+pass), and replays the whole step from a CUDA graph.  Here a 3-layer step run
+that way must leave every bias and every gradient bit-identical to the same
+layers run one after the other (plain lei_apply after each layer).
 """
 import os
 import sys

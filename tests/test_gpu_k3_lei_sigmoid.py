@@ -172,3 +172,83 @@ def test_lei_shapes_and_ragged_batches(qb, orc, N, E, k, bt):
         sl = slice(m * bt_eff, min(N, (m + 1) * bt_eff))
         want, _, _ = orc.lei(g0[sl], t[sl], 0.5)
         assert np.max(np.abs(got[sl] - want)) <= LEI_ABS_TOL
+
+
+@pytest.mark.parametrize("N,E,k,bt", [(1, 32, 1, 0), (1000, 64, 6, 333), (4097, 512, 15, 1024),
+                                      (70001, 256, 6, 4099)])
+def test_lei_rho_then_apply_equals_inject(qb, orc, N, E, k, bt):
+    # The two halves on one stream give lei_inject's result bit for bit;
+    # lei_apply alone is grad + workspace[batch(row)] in binary32 for every
+    # element, checked against numpy on the workspace it was given.  Batch
+    # sizes that are not multiples of a CTA's rows put batch boundaries
+    # inside a CTA's run.
+    topk = inputs.random_topk(N, E, k, seed=N + 7, device="cuda")
+    topk[: N // 4] = torch.arange(k, dtype=torch.int32, device="cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(N + 7)
+    grad = torch.randn(N, E, generator=g, device="cuda") * 1e-3
+    g0 = grad.cpu().numpy()
+    bt_eff = bt or N
+    nb = (N + bt_eff - 1) // bt_eff
+    ws_a = torch.empty(nb, E, dtype=torch.float32, device="cuda")
+    ws_b = torch.empty_like(ws_a)
+    grad_b = grad.clone()
+    qb.lei_inject(grad, topk, 0.5, ws_a, batch_tokens=bt)
+    qb.lei_rho(topk, E, 0.5, ws_b, batch_tokens=bt)
+    qb.lei_apply(grad_b, ws_b, batch_tokens=bt)
+    torch.cuda.synchronize()
+    assert torch.equal(ws_a, ws_b)
+    assert torch.equal(grad.view(torch.int32), grad_b.view(torch.int32))
+    c = ws_b.cpu().numpy()
+    rows = np.arange(N) // bt_eff
+    want = (g0 + c[rows]).astype(np.float32)
+    assert np.array_equal(grad_b.cpu().numpy().view(np.int32), want.view(np.int32))
+    t = topk.cpu().numpy()
+    got = grad_b.cpu().numpy()
+    for m in range(nb):
+        sl = slice(m * bt_eff, min(N, (m + 1) * bt_eff))
+        want_m, _, _ = orc.lei(g0[sl], t[sl], 0.5)
+        assert np.max(np.abs(got[sl] - want_m)) <= LEI_ABS_TOL
+
+
+@pytest.mark.parametrize("N,E,bt", [(1, 32, 0), (1000, 64, 333), (4097, 512, 1024),
+                                    (70001, 256, 4099), (524288, 256, 32768)])
+def test_lei_apply_overlap_equals_apply(qb, N, E, bt):
+    # The bulk-copy variant gives lei_apply's result bit for bit, alone and
+    # launched behind a routing pass that it runs beside; the routing pass's
+    # own outputs are unchanged by the kernel running next to it.
+    g = torch.Generator(device="cuda")
+    g.manual_seed(N + 11)
+    grad = torch.randn(N, E, generator=g, device="cuda") * 1e-3
+    bt_eff = bt or N
+    nb = (N + bt_eff - 1) // bt_eff
+    ws = torch.randn(nb, E, generator=g, device="cuda") * 1e-5
+    want = grad.clone()
+    qb.lei_apply(want, ws, batch_tokens=bt)
+    alone = grad.clone()
+    qb.lei_apply_overlap(alone, ws, batch_tokens=bt)
+    torch.cuda.synchronize()
+    assert torch.equal(alone.view(torch.int32), want.view(torch.int32))
+    # behind a routing pass over other data
+    w = inputs.scaled(inputs.WORKLOADS["full_step"], n_micro=2)
+    lg = torch.empty(w.n_pool, w.E, dtype=torch.float32, device="cuda")
+    bias, _ = inputs.router_layer(w, inputs.seed_for("full_step", 2), device="cuda", out=lg)
+    outs = []
+    for overlap in (False, True):
+        hist = torch.zeros(w.E, 256, dtype=torch.int32, device="cuda")
+        keys = torch.empty(w.n_pool, w.E, dtype=torch.int16, device="cuda")
+        topk = torch.empty(w.n_pool, w.k, dtype=torch.int32, device="cuda")
+        behind = grad.clone()
+        torch.cuda.synchronize()
+        qb.qb_route_hist_hi(lg, bias, w.k, hist, keys_out=keys, topk_out=topk)
+        if overlap:
+            qb.lei_apply_overlap(behind, ws, batch_tokens=bt)
+            hist_after = hist.clone()  # ordered after both kernels
+        torch.cuda.synchronize()
+        outs.append((hist, keys, topk))
+        if overlap:
+            assert torch.equal(behind.view(torch.int32), want.view(torch.int32))
+            assert torch.equal(hist_after, hist)
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
+    assert qb.device_status() == 0

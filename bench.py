@@ -42,12 +42,12 @@ METRIC = "QB routed tokens/s per layer (E=256,k=6, 2-pass EQB) on 1 GB300; % of 
 # launch on a 524288-token layer, from the ncu capture summarised in
 # profiles/route_kernel_hi_one_layer.md.  Reported only while the kernel's
 # sources hash to the value they had when the counters were taken.
-ROUTE_TRAFFIC = {"sha1": "b2645c7e52c3878e148156b8476fbf9e83b2f1bd", "tokens": 524288,
-                 "bytes": (537.022464 + 245.423872) * 1e6}
+ROUTE_TRAFFIC = {"sha1": "3e4d4f59d2ed626bde6df758fd648c9a4b198f25", "tokens": 524288,
+                 "bytes": (537.009408 + 245.643264) * 1e6}
 ROUTE_SOURCES = ("qb_route.cuh", "qb_device.cuh", "qb_route_hi.cu")
 # Warp instructions of the same capture (smsp__inst_executed.sum), for the
 # issue-rate roofline of this issue-bound kernel; same hash guard.
-ROUTE_INSTR = {"tokens": 524288, "warp_instructions": None}
+ROUTE_INSTR = {"tokens": 524288, "warp_instructions": 177414280}
 UNIT = "tokens/s/layer"
 WORKLOAD = "full_step"
 
@@ -660,7 +660,8 @@ def main():
                        "layers": fs.L, "tokens_per_layer": n, "E": E, "k": k,
                        "parallelism": f"replicas x{world} (token shards, no collective)",
                        "cuda_graph": not args.no_graph,
-                       "l2": "inputs (48 GiB) far larger than L2; no flush"},
+                       "l2": f"resident logits + gradients ({2 * fs.L * n * E * 4 / 2**30:g} GiB) "
+                             "larger than L2 (129 MB); no flush"},
             "eqb_only": {"value": eqb_value, "unit": UNIT, "ms_per_step": ms_eqb / args.steps},
             # whole-path HBM roofline: algorithmic bytes of every kernel of a layer
             # (hi pass 1560 B/token, lo pass 512, LEI counts 24, LEI apply 2048)

@@ -197,8 +197,9 @@ class FullStep:
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record()
+        # the top-k sets are LEI's input only: EQB alone does not produce them
         qb.qb_route_hist_hi(lg, self.bias[l], w.k, self.hist_hi[l], keys_out=self.keys,
-                            topk_out=self.topk[j])
+                            topk_out=self.topk[j] if lei else None)
         if time_hi:
             e1.record()
             self.hi_events.append((e0, e1))
@@ -585,8 +586,8 @@ def main():
     n, E, k = w.n_pool, w.E, w.k
     hi_bytes = n * E * (4 + 2) + n * k * 4   # logits read, keys write, top-k write
     hi_avg_ms = statistics.mean(hi_ms) if hi_ms else float("nan")
-    eqb_bytes = hi_bytes + n * E * 2                      # + the lo pass over the keys
-    step_bytes = eqb_bytes + n * k * 4 + n * E * 4 * 2    # + LEI counts and grad read/write
+    eqb_bytes = n * E * (4 + 2) + n * E * 2               # hi pass without top-k + lo pass
+    step_bytes = hi_bytes + n * E * 2 + n * k * 4 + n * E * 4 * 2  # + LEI counts, grad R/W
     achieved = hi_bytes / (hi_avg_ms / 1e3) / 1e9
 
     # end to end through host buffers: per layer H2D logits + grad, D2H grad + bias

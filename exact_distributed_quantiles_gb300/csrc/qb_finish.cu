@@ -32,7 +32,7 @@ namespace {
 constexpr int kLoThreads = 256;
 constexpr int kLoEG = 32;                // experts per CTA slice
 constexpr int kLoRowW = 257;             // words per expert row in shared memory
-constexpr int kLoSmemWords = kLoEG * kLoRowW;
+constexpr int kLoSmemWords = (kLoEG + 1) * kLoRowW;  // + a discard row
 
 // No "memory" clobber: nothing reads the counters before the __syncthreads
 // that precedes the flush, and without it the compiler may schedule the
@@ -64,10 +64,15 @@ __global__ void __launch_bounds__(kLoThreads)
   for (int i = 0; i < 4; ++i)
     spat[i] = ((uint32_t)(sel[eg * kLoEG + el0 + 2 * i] & 0xFF) << 8) |
               ((uint32_t)(sel[eg * kLoEG + el0 + 2 * i + 1] & 0xFF) << 24);
+  // an expert without a selected bin (sel outside [0, 256)) counts into the
+  // extra row kLoEG, which is never flushed
   const uint32_t hb = (uint32_t)__cvta_generic_to_shared(h);
   uint32_t ebase[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) ebase[j] = hb + 4u * (uint32_t)((el0 + j) * kLoRowW);
+  for (int j = 0; j < 8; ++j) {
+    const int sj = sel[eg * kLoEG + el0 + j];
+    ebase[j] = hb + 4u * (uint32_t)((sj >= 0 && sj < 256 ? el0 + j : kLoEG) * kLoRowW);
+  }
   __syncthreads();
 
   const int64_t n_rows = r_end > r_begin ? r_end - r_begin : 0;

@@ -210,3 +210,34 @@ def test_eqb_all_expert_counts(qb, orc, E, k):
     res = _eqb_gpu(qb, mbs, bias, w.k)
     ref = orc.eqb_global_batch([host_logits(m) for m in mbs], bias.cpu().numpy(), w.k)
     _check_eqb(res, ref)
+
+
+def _lo_keys(N, E, seed):
+    # keys concentrated on a few hi bytes (so that many fall in the selected
+    # bin), every lo byte, and some keys in bins 0x00 and 0xFF
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    hi = torch.randint(0, 4, (N, E), generator=g, device="cuda") + 0x80
+    hi[torch.rand(N, E, generator=g, device="cuda") < 0.05] = 0xFF
+    hi[torch.rand(N, E, generator=g, device="cuda") < 0.05] = 0x00
+    lo = torch.randint(0, 256, (N, E), generator=g, device="cuda")
+    keys = (hi * 256 + lo).to(torch.int32).to(torch.int16)
+    sel = torch.randint(0x80, 0x84, (E,), generator=g, device="cuda").to(torch.int32)
+    sel[::7] = -1                 # no selected bin
+    sel[3::11] = 0xFF
+    sel[5::13] = 0x00
+    return keys, sel
+
+
+@pytest.mark.parametrize("E", [32, 64, 128, 256, 512])
+@pytest.mark.parametrize("N", [1, 31, 4097])
+def test_keys_hist_lo_equals_definition(qb, orc, E, N):
+    # The lo pass from stored keys equals the oracle's direct count on keys
+    # spread over bins 0x00, 0x80-0x83 and 0xFF, with sel = -1 (no selected
+    # bin) counting nothing and sel = 0x00 / 0xFF counting the edge bins.
+    keys, sel = _lo_keys(N, E, seed=E * 7 + N)
+    want = orc.hist_lo(np_u16(keys), sel.cpu().numpy())
+    h = torch.zeros(E, 256, dtype=torch.int32, device="cuda")
+    qb.qb_keys_hist_lo(keys, sel, h)
+    torch.cuda.synchronize()
+    assert np.array_equal(h.cpu().numpy(), want)

@@ -5,16 +5,22 @@
 // scores from hidden states; the histogram passes then run on those scores
 // ("Implementation": the fused path extends the existing router kernel).
 //
-// One CTA computes a 128 x 256 tile of logits (all experts of 128 tokens):
+// One persistent CTA per SM walks tiles of 128 x 256 logits (all experts of
+// 128 tokens), tile = blockIdx.x + i * gridDim.x:
 //   warp 0      TMA producer: hidden tile 128 x 64 and W^T tile 256 x 64 per
 //               stage (bf16, 128-byte swizzle) into a 4-deep ring;
-//   warp 1      allocates 256 TMEM columns; one lane issues tcgen05.mma
-//               (M=128, N=256, K=16) four times per stage and commits each
-//               stage back to the producer, and the last one to the epilogue;
-//   warps 2-5   epilogue: tcgen05.ld 32 lanes x 32 columns at a time, fp32
-//               stores of the logits.
-// Every mbarrier wait is bounded; a timeout sets the device status flag and
-// the CTA still frees its TMEM before returning.
+//   warp 1      allocates 512 TMEM columns (two accumulators); one lane issues
+//               tcgen05.mma (M=128, N=256, K=16) four times per stage into
+//               accumulator (local tile index & 1), commits each stage back to
+//               the producer and each finished tile to its epilogue;
+//   warps 2-9   two epilogue warpgroups, warpgroup b draining accumulator b
+//               (tcgen05.ld 32 lanes x 32 columns at a time, fp32 stores), so
+//               that one tile's stores overlap the next tile's MMAs.
+// At full MMA rate the hidden-state slices (16 KB per 0.33 us per SM) would
+// need more than the HBM bandwidth: the kernel is bound by HBM, not by the
+// tensor cores (W^T comes from L2).  Every mbarrier wait is bounded; a
+// timeout sets the device status flag and the CTA still frees its TMEM
+// before returning.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -28,13 +34,14 @@ namespace qb {
 namespace {
 
 constexpr int kBM = 128;        // tokens per tile (TMEM lanes)
-constexpr int kBN = 256;        // experts per tile (TMEM columns)
+constexpr int kBN = 256;        // experts per tile (TMEM columns per accumulator)
 constexpr int kBK = 64;         // K per stage: one 128-byte swizzle row of bf16
 constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK * 2;  // 16 KB
 constexpr int kBBytes = kBN * kBK * 2;  // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
 
 constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN);
@@ -55,72 +62,96 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* sbase = smem_raw + (base - raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sbase + kStages * kStageBytes);
-  uint64_t* full = bars;                 // [kStages]
-  uint64_t* empty = bars + kStages;      // [kStages]
-  uint64_t* accum = bars + 2 * kStages;  // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 1);
+  uint64_t* full = bars;                  // [kStages]
+  uint64_t* empty = bars + kStages;       // [kStages]
+  uint64_t* tfull = bars + 2 * kStages;   // [2]
+  uint64_t* tempty = tfull + 2;           // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
 
-  const int warp = threadIdx.x >> 5;
+  const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
   const int lane = threadIdx.x & 31;
-  const int64_t m0 = (int64_t)blockIdx.x * kBM;
   const int ktiles = g.K / kBK;
+  const int64_t n_tiles = (g.M + kBM - 1) / kBM;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full + s, 1);
       mbar_init(empty + s, 1);
     }
-    mbar_init(accum, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull + b, 1);
+      mbar_init(tempty + b, kEpiWarps / 2 * 32);
+    }
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kBN);
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 2 * kBN);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  bool ok = true;
 
   if (warp == 0) {
     if (lane == 0) {
-      for (int kt = 0; kt < ktiles && ok; ++kt) {
-        const int s = kt % kStages;
-        const uint32_t round = (uint32_t)(kt / kStages);
-        if (kt >= kStages) ok = mbar_wait_bounded(empty + s, (round - 1) & 1u, g.status);
-        if (!ok) break;
-        const uint32_t sa = base + (uint32_t)(s * kStageBytes);
-        mbar_arrive_expect_tx(full + s, (uint32_t)kStageBytes);
-        tma_load_2d(sa, &map_a, kt * kBK, (int)m0, smem_u32(full + s));
-        tma_load_2d(sa + kABytes, &map_b, kt * kBK, 0, smem_u32(full + s));
+      uint32_t gk = 0;
+      bool ok = true;
+      for (int64_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        for (int kt = 0; kt < ktiles; ++kt, ++gk) {
+          const int s = (int)(gk % kStages);
+          const uint32_t round = gk / kStages;
+          if (gk >= (uint32_t)kStages && !mbar_wait_bounded(empty + s, (round - 1) & 1u, g.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = base + (uint32_t)(s * kStageBytes);
+          mbar_arrive_expect_tx(full + s, (uint32_t)kStageBytes);
+          tma_load_2d(sa, &map_a, kt * kBK, (int)(tile * kBM), smem_u32(full + s));
+          tma_load_2d(sa + kABytes, &map_b, kt * kBK, 0, smem_u32(full + s));
+        }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      for (int kt = 0; kt < ktiles && ok; ++kt) {
-        const int s = kt % kStages;
-        ok = mbar_wait_bounded(full + s, (uint32_t)(kt / kStages) & 1u, g.status);
-        if (!ok) break;
+      uint32_t gk = 0, lt = 0;
+      bool ok = true;
+      for (int64_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++lt) {
+        const uint32_t b = lt & 1u, use = lt >> 1;
+        if (use >= 1 && !mbar_wait_bounded(tempty + b, (use - 1) & 1u, g.status)) break;
         tc_fence_after();
-        const uint32_t sa = base + (uint32_t)(s * kStageBytes);
+        const uint32_t d = tmem + b * (uint32_t)kBN;
+        for (int kt = 0; kt < ktiles; ++kt, ++gk) {
+          const int s = (int)(gk % kStages);
+          if (!mbar_wait_bounded(full + s, (gk / kStages) & 1u, g.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = base + (uint32_t)(s * kStageBytes);
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          // the 16-element K slice starts 32 bytes further along the row
-          const uint64_t ad = smem_desc_sw128(sa + 32u * kk);
-          const uint64_t bd = smem_desc_sw128(sa + kABytes + 32u * kk);
-          tc_mma(tmem, ad, bd, kIdesc, (kt > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // the 16-element K slice starts 32 bytes further along the row
+            const uint64_t ad = smem_desc_sw128(sa + 32u * kk);
+            const uint64_t bd = smem_desc_sw128(sa + kABytes + 32u * kk);
+            tc_mma(d, ad, bd, kIdesc, (kt > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(smem_u32(empty + s));  // frees the stage once these MMAs are done
         }
-        tc_commit(smem_u32(empty + s));  // frees the stage once these MMAs are done
+        if (ok) tc_commit(smem_u32(tfull + b));  // all MMAs of the tile
       }
-      tc_commit(smem_u32(accum));  // all MMAs of the tile
     }
   } else {
-    // epilogue warps 2..5: warp w reads TMEM lanes 32*(w%4) .. +31
+    // epilogue: warpgroup wg drains accumulator wg; warp w reads TMEM lanes
+    // 32*(w%4) .. +31 (one token each)
+    const int wg = (warp - 2) >> 2;
     const int q = warp & 3;
-    ok = mbar_wait_bounded(accum, 0u, g.status);
-    ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective
-    tc_fence_after();
-    if (ok) {
-      const int64_t row = m0 + 32 * q + lane;
-      const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
+    uint32_t use = 0;
+    for (int64_t tile = blockIdx.x + (int64_t)wg * gridDim.x; tile < n_tiles;
+         tile += 2 * (int64_t)gridDim.x, ++use) {
+      bool ok = mbar_wait_bounded(tfull + wg, use & 1u, g.status);
+      ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective
+      if (!ok) break;
+      tc_fence_after();
+      const int64_t row = tile * kBM + 32 * q + lane;
+      const uint32_t lane_base = tmem + (uint32_t)(wg * kBN) + ((uint32_t)(32 * q) << 16);
 #pragma unroll 1
       for (int c0 = 0; c0 < kBN; c0 += 32) {
         uint32_t r[32];
@@ -133,13 +164,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
         }
       }
+      tc_fence_before();
+      mbar_arrive(tempty + wg);  // the accumulator may be overwritten
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kBN);
+    tmem_dealloc(tmem, 2 * kBN);
   }
 }
 
@@ -196,7 +229,9 @@ int launch_router_gemm(const void* hidden, const void* w_t, int64_t M, int K, in
     attr = true;
   }
   const int64_t tiles = (M + kBM - 1) / kBM;
-  router_gemm_kernel<<<(unsigned)tiles, kThreads, kSmemBytes, stream>>>(ma, mb, g);
+  int64_t grid = sm_count();
+  if (grid > tiles) grid = tiles;
+  router_gemm_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(ma, mb, g);
   return launch_status();
 }
 

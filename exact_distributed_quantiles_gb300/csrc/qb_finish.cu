@@ -22,17 +22,19 @@ namespace {
 // counters and the flush issues few global atomics (merging 152 full
 // per-SM histograms through L2 atomics would cost more than the pass itself).
 // Four lanes cover one row slice (16 bytes = 8 keys each), a warp covers 8
-// rows per load; loads are double-buffered in registers.  Every key issues one
-// shared increment without branching: with t = key ^ (sel << 8) the low byte
-// is the key's, the high byte zero exactly when the key is in the selected
-// bin, so min(t, 256) is the counter's index, or 256 -- the 257th word of the
-// expert's row, never flushed -- for every other key.  Layout: counter
-// (e, lo) at word e * 257 + lo (257 spreads the experts over the banks).
+// rows per load.  Loads run one iteration ahead in two register sets used in
+// turn (no copies); iterations whose rows are all in range need no bounds
+// checks.  Every key issues one shared increment without branching: with
+// t = key ^ (sel << 8) the low byte is the key's, the high byte zero exactly
+// when the key is in the selected bin, so min(t, 256) is the counter's index,
+// or 256 -- the 257th word of the expert's row, never flushed -- for every
+// other key.  Layout: counter (e, lo) at word e * 257 + lo (257 spreads the
+// experts over the banks).
 // ------------------------------------------------------------------------
 constexpr int kLoThreads = 256;
 constexpr int kLoEG = 32;                // experts per CTA slice
 constexpr int kLoRowW = 257;             // words per expert row in shared memory
-constexpr int kLoSmemWords = (kLoEG + 1) * kLoRowW;  // + a discard row
+constexpr int kLoSmemWords = kLoEG * kLoRowW;
 
 // No "memory" clobber: nothing reads the counters before the __syncthreads
 // that precedes the flush, and without it the compiler may schedule the
@@ -41,7 +43,7 @@ __device__ __forceinline__ void red_shared1(uint32_t addr) {
   asm volatile("red.shared.add.u32 [%0], 1;" ::"r"(addr));
 }
 
-__global__ void __launch_bounds__(kLoThreads)
+__global__ void __launch_bounds__(kLoThreads, 4)
     keys_hist_lo_kernel(const uint16_t* __restrict__ keys, int64_t N, int E,
                         const int32_t* __restrict__ sel, int32_t* __restrict__ hist_lo,
                         int64_t rows_per_cta) {
@@ -64,56 +66,76 @@ __global__ void __launch_bounds__(kLoThreads)
   for (int i = 0; i < 4; ++i)
     spat[i] = ((uint32_t)(sel[eg * kLoEG + el0 + 2 * i] & 0xFF) << 8) |
               ((uint32_t)(sel[eg * kLoEG + el0 + 2 * i + 1] & 0xFF) << 24);
-  // an expert without a selected bin (sel outside [0, 256)) counts into the
-  // extra row kLoEG, which is never flushed
   const uint32_t hb = (uint32_t)__cvta_generic_to_shared(h);
   uint32_t ebase[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int sj = sel[eg * kLoEG + el0 + j];
-    ebase[j] = hb + 4u * (uint32_t)((sj >= 0 && sj < 256 ? el0 + j : kLoEG) * kLoRowW);
-  }
+  for (int j = 0; j < 8; ++j) ebase[j] = hb + 4u * (uint32_t)((el0 + j) * kLoRowW);
   __syncthreads();
 
   const int64_t n_rows = r_end > r_begin ? r_end - r_begin : 0;
   const uint16_t* base = keys + r_begin * E + eg * kLoEG + el0;
   constexpr int kU = 4;                           // 8-row blocks per warp in flight
   const int64_t stride = (int64_t)kWarps * 8 * kU;  // rows per CTA iteration
-  uint4 cur[kU];
-  int64_t r0 = (int64_t)warp * 8 * kU + rsub;
+  // rows r_first + it * stride + 8 q; in the first n_full iterations all kU
+  // rows are in range (no checks, loads two iterations deep without copies)
+  const int64_t r_first = (int64_t)warp * 8 * kU + rsub;
+  const int64_t last_need = r_first + 8 * (kU - 1);
+  const int64_t n_full = n_rows > last_need ? (n_rows - 1 - last_need) / stride + 1 : 0;
+  const uint4* p4 = reinterpret_cast<const uint4*>(base + r_first * E);
+  const int64_t q4 = E;                 // uint4 between q blocks (8 rows x E/8)
+  const int64_t it4 = stride * (E / 8);  // uint4 per iteration
+  auto load = [&](uint4 (&v)[kU], const uint4* p) {
+#pragma unroll
+    for (int q = 0; q < kU; ++q) v[q] = __ldcs(p + q * q4);
+  };
+  auto count = [&](const uint4 (&v)[kU]) {
+#pragma unroll
+    for (int q = 0; q < kU; ++q) {
+      const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t x = w[i] ^ spat[i];  // selected hi bytes become 0
+        red_shared1(ebase[2 * i] + 4u * min(x & 0xFFFFu, 256u));
+        red_shared1(ebase[2 * i + 1] + 4u * min(x >> 16, 256u));
+      }
+    }
+  };
+  uint4 va[kU], vb[kU];
+  int64_t it = 0;
+  if (n_full > 0) load(va, p4);
+  for (; it + 1 < n_full; it += 2) {
+    load(vb, p4 + (it + 1) * it4);
+    count(va);
+    if (it + 2 < n_full) load(va, p4 + (it + 2) * it4);
+    count(vb);
+  }
+  if (it < n_full) {
+    count(va);
+    ++it;
+  }
+  // the partial last iteration
+  const int64_t r0 = r_first + it * stride;
 #pragma unroll
   for (int q = 0; q < kU; ++q) {
-    const int64_t r = r0 + 8 * q;
-    cur[q] = r < n_rows ? __ldcs(reinterpret_cast<const uint4*>(base + r * E))
-                        : make_uint4(0u, 0u, 0u, 0u);
-  }
-  for (; r0 < n_rows; r0 += stride) {
-    uint4 nxt[kU];
+    if (r0 + 8 * q < n_rows) {
+      const uint4 v = __ldcs(reinterpret_cast<const uint4*>(base + (r0 + 8 * q) * E));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int q = 0; q < kU; ++q) {
-      const int64_t r = r0 + stride + 8 * q;
-      nxt[q] = r < n_rows ? __ldcs(reinterpret_cast<const uint4*>(base + r * E))
-                          : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int q = 0; q < kU; ++q) {
-      if (r0 + 8 * q < n_rows) {
-        const uint32_t w[4] = {cur[q].x, cur[q].y, cur[q].z, cur[q].w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t x = w[i] ^ spat[i];  // selected hi bytes become 0
-          red_shared1(ebase[2 * i] + 4u * min(x & 0xFFFFu, 256u));
-          red_shared1(ebase[2 * i + 1] + 4u * min(x >> 16, 256u));
-        }
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t x = w[i] ^ spat[i];
+        red_shared1(ebase[2 * i] + 4u * min(x & 0xFFFFu, 256u));
+        red_shared1(ebase[2 * i + 1] + 4u * min(x >> 16, 256u));
       }
-      cur[q] = nxt[q];
     }
   }
   __syncthreads();
+  // an expert without a selected bin (sel outside [0, 256)) counted the keys
+  // of bin sel & 0xFF; its counts are dropped here
   for (int i = threadIdx.x; i < kLoEG * 256; i += kLoThreads) {
     const int el = i >> 8, lo = i & 255;
     const uint32_t c = h[el * kLoRowW + lo];
-    if (c) atomicAdd(hist_lo + (int64_t)(eg * kLoEG + el) * 256 + lo, (int)c);
+    const int se = sel[eg * kLoEG + el];
+    if (c && se >= 0 && se < 256) atomicAdd(hist_lo + (int64_t)(eg * kLoEG + el) * 256 + lo, (int)c);
   }
 }
 

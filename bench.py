@@ -176,7 +176,7 @@ class FullStep:
         self.ev_rho = [torch.cuda.Event() for _ in range(2)]
         self.pending = None  # (grad, slot) of a layer whose grad update is still to be enqueued
         self.R = qb.rank(n, E, k)
-        self.launches_per_layer = {"eqb": 5, "lei": 2}
+        self.launches_per_layer = {"eqb": 4, "lei": 2}
         self.hi_events = []
 
     def layer(self, l, logits=None, grad=None, lei=True, time_hi=False, join=False):

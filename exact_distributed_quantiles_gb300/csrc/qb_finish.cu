@@ -8,11 +8,15 @@
 //   at k/E, subtract the mean; K3 range [min b - 1, max b + 1]) and
 //   "Implementation" (update bias and bounds once, reset the histogram in
 //   place).
+#include <cooperative_groups.h>
+
 #include "qb_device.cuh"
 #include "qb_internal.h"
 
 namespace qb {
 namespace {
+
+namespace cg = cooperative_groups;
 
 // ------------------------------------------------------------------------
 // Lo-byte histogram from stored keys.
@@ -160,13 +164,10 @@ __global__ void __launch_bounds__(256) select_hi_kernel(const int32_t* __restric
                                                         long long r, int32_t* __restrict__ sel,
                                                         int32_t* __restrict__ r_lo) {
   __shared__ long long tmp[8];
-  __shared__ long long cum_s[256];
   const int j = blockIdx.x;
   const int b = threadIdx.x;
   const long long c = hist_hi[(int64_t)j * 256 + b];
   const long long cum = block_inclusive_scan256(c, tmp);
-  cum_s[b] = cum;
-  __syncthreads();
   const long long before = cum - c;
   if (cum >= r && before < r) {
     sel[j] = b;
@@ -179,107 +180,177 @@ __global__ void __launch_bounds__(256) select_hi_kernel(const int32_t* __restric
 }
 
 // ------------------------------------------------------------------------
-// EQB finalize, two kernels.
-// eqb_lo_select_kernel: one CTA (256 threads) per expert.  Block scan of the
-//   lo histogram row, first bin reaching r_lo, key -> bf16 value q_j written
-//   to bias_out[j] (a staging slot), key to qkey_out; with reset the CTA then
-//   zeroes its own hist_hi and hist_lo rows in place.
-// eqb_center_kernel: one CTA.  mu = (sum_j q_j in fp64, ascending j) / E,
+// EQB finalize: one cluster of 8 CTAs (1024 threads each), CTA c owning the
+// experts [c*E/8, (c+1)*E/8), one warp per expert:
+//   the warp scans the expert's lo histogram (8 consecutive bins per lane, a
+//   shuffle scan over the lanes) for the first bin reaching r_lo, decodes the
+//   key (sel << 8) | lo to the fp32 value q_j of its bf16 number, and with
+//   reset zeroes the expert's hist_hi and hist_lo rows in place;
+//   mu = (sum_j q_j in fp64) / E.  A bf16 number is m * 2^(e - 134) with an
+//   8-bit m (e the biased exponent, 1 for subnormals), so when the non-zero
+//   q_j's exponents span at most 36 (none inf or NaN) the sum is the integer
+//   S = sum_j +-m_j * 2^(e_j - e_min) < 2^53 times 2^(e_min - 134): every CTA
+//   sends its partial integer sum (relative to its own e_min) with its
+//   exponent range in one cluster exchange, and mu = S * 2^(e_min - 134) / E
+//   is exact -- the value of the ascending serial fp64 sum, which is then
+//   exact too.  Otherwise every CTA sums all E values serially in ascending
+//   j in fp64, read over distributed shared memory;
 //   bias_out[j] = RN32(q_j - mu).
 // ------------------------------------------------------------------------
+constexpr int kFinCluster = 8;
+constexpr int kFinThreads = 1024;
+constexpr int kNoExp = 1 << 20;  // exponent-range sentinel of a CTA without non-zero q
+
 __device__ __forceinline__ float key_decode(uint32_t key) {
   const uint32_t h = (key & 0x8000u) ? (key ^ 0x8000u) : (key ^ 0xFFFFu);
   return __uint_as_float((h & 0xFFFFu) << 16);
 }
 
-__global__ void __launch_bounds__(256) eqb_lo_select_kernel(
-    int32_t* __restrict__ hist_hi, int32_t* __restrict__ hist_lo, const int32_t* __restrict__ sel,
-    const int32_t* __restrict__ r_lo, float* __restrict__ bias_out,
-    uint16_t* __restrict__ qkey_out, int reset) {
-  __shared__ long long tmp[8];
-  __shared__ int lo_s;
-  const int j = blockIdx.x;
-  const int b = threadIdx.x;
-  const int sj = sel[j];
-  const long long target = r_lo[j];
-  const long long c = hist_lo[(int64_t)j * 256 + b];
-  if (b == 0) lo_s = -1;
-  const long long cum = block_inclusive_scan256(c, tmp);  // contains __syncthreads
-  if (cum >= target && cum - c < target) lo_s = b;
-  __syncthreads();
-  if (b == 0) {
-    const int lo = lo_s;
-    if (sj >= 0 && lo >= 0) {
-      const uint32_t key = ((uint32_t)sj << 8) | (uint32_t)lo;
-      bias_out[j] = key_decode(key);
-      if (qkey_out) qkey_out[j] = (uint16_t)key;
-    } else {
-      bias_out[j] = __int_as_float(0x7FC00000);  // rank beyond the pooled count
-      if (qkey_out) qkey_out[j] = 0;
-    }
-  }
-  if (reset) {
-    hist_lo[(int64_t)j * 256 + b] = 0;
-    hist_hi[(int64_t)j * 256 + b] = 0;
-  }
-}
-
-// Sum of E <= 512 bf16-valued fp32 numbers in fp64, equal to the ascending
-// serial fp64 sum.  When the non-zero values' binary exponents span at most
-// 36, every partial sum in any order is exact (8 significant bits per value,
-// 1 + 9 more for the magnitude of up to 512 terms: 36 + 17 <= 53 bits), so a
-// parallel tree gives the serial result; otherwise one thread sums serially.
-__device__ double bf16_values_sum_fp64(const float* q_s, int E, double* red, int* emin_s,
-                                       int* emax_s, int* bad_s) {
-  const int tid = threadIdx.x;
-  if (tid == 0) {
-    *emin_s = 1 << 20;
-    *emax_s = -(1 << 20);
-    *bad_s = 0;
-  }
-  __syncthreads();
-  for (int j = tid; j < E; j += blockDim.x) {
-    const uint32_t u = __float_as_uint(q_s[j]);
-    const int ex = (int)((u >> 23) & 0xFFu);
-    if (ex == 0xFF) atomicOr(bad_s, 1);
-    if ((u & 0x7FFFFFFFu) != 0) {
-      atomicMin(emin_s, ex);
-      atomicMax(emax_s, ex);
-    }
-  }
-  __syncthreads();
-  const bool tree = (*bad_s == 0) && (*emax_s - *emin_s <= 36);
-  double v = 0.0;
-  if (tree) {
-    for (int j = tid; j < E; j += blockDim.x) v = __dadd_rn(v, (double)q_s[j]);
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) v = __dadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
-    if ((tid & 31) == 0) red[tid >> 5] = v;
-    __syncthreads();
-    if (tid == 0) {
-      double s = 0.0;
-      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s = __dadd_rn(s, red[w]);
-      red[0] = s;
-    }
-  } else if (tid == 0) {
-    double s = 0.0;
-    for (int j = 0; j < E; ++j) s = __dadd_rn(s, (double)q_s[j]);
-    red[0] = s;
-  }
-  __syncthreads();
-  return red[0];
-}
-
-__global__ void __launch_bounds__(512) eqb_center_kernel(float* __restrict__ bias_out, int E) {
-  __shared__ float q_s[512];
-  __shared__ double red[16];
+__global__ void __cluster_dims__(kFinCluster, 1, 1) __launch_bounds__(kFinThreads)
+    eqb_finalize_kernel(int32_t* __restrict__ hist_hi, int32_t* __restrict__ hist_lo,
+                        const int32_t* __restrict__ sel, const int32_t* __restrict__ r_lo, int E,
+                        int log2E, float* __restrict__ bias_out, uint16_t* __restrict__ qkey_out,
+                        int reset) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  __shared__ float q_s[64];
   __shared__ int emin_s, emax_s, bad_s;
-  for (int j = threadIdx.x; j < E; j += blockDim.x) q_s[j] = bias_out[j];
+  __shared__ long long part_s;
+  __shared__ double mu_s;
+  const int per = E / kFinCluster;  // experts of this CTA (4 .. 64)
+  const int j0 = rank * per;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int jl = warp; jl < per; jl += kFinThreads / 32) {
+    const int j = j0 + jl;
+    int32_t* row = hist_lo + (int64_t)j * 256;
+    int c[8];
+    int t = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      c[i] = row[8 * lane + i];
+      t += c[i];
+    }
+    int incl = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int target = r_lo[j];
+    const unsigned hit = __ballot_sync(0xffffffffu, target >= 1 && incl >= target);
+    int lo = -1;
+    if (hit) {
+      const int src = __ffs((int)hit) - 1;
+      int off = 7, cum = incl - t;
+#pragma unroll
+      for (int i = 0, found = 0; i < 8; ++i) {  // the first i with cum + c[0..i] >= target
+        cum += c[i];
+        if (!found && cum >= target) {
+          off = i;
+          found = 1;
+        }
+      }
+      lo = __shfl_sync(0xffffffffu, 8 * src + off, src);
+    }
+    if (lane == 0) {
+      const int sj = sel[j];
+      if (sj >= 0 && sj < 256 && lo >= 0) {
+        const uint32_t key = ((uint32_t)sj << 8) | (uint32_t)lo;
+        q_s[jl] = key_decode(key);
+        if (qkey_out) qkey_out[j] = (uint16_t)key;
+      } else {
+        q_s[jl] = __int_as_float(0x7FC00000);  // rank beyond the pooled count
+        if (qkey_out) qkey_out[j] = 0;
+      }
+    }
+    if (reset) {
+      int32_t* rh = hist_hi + (int64_t)j * 256;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        row[32 * i + lane] = 0;
+        rh[32 * i + lane] = 0;
+      }
+    }
+  }
   __syncthreads();
-  const double mu = __ddiv_rn(bf16_values_sum_fp64(q_s, E, red, &emin_s, &emax_s, &bad_s),
-                              (double)E);
-  for (int j = threadIdx.x; j < E; j += blockDim.x)
-    bias_out[j] = __double2float_rn(__dsub_rn((double)q_s[j], mu));
+  if (warp == 0) {
+    // this CTA's exponent range and integer partial sum (relative to its e_min)
+    uint32_t u[2];
+    int ex[2], nz[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int jl = lane + 32 * h;
+      u[h] = jl < per ? __float_as_uint(q_s[jl]) : 0u;
+      ex[h] = (int)((u[h] >> 23) & 0xFFu);
+      nz[h] = (u[h] & 0x7FFFFFFFu) != 0;
+    }
+    const int bad = __reduce_or_sync(0xffffffffu, (ex[0] == 0xFF) | (ex[1] == 0xFF));
+    const int emin = (int)__reduce_min_sync(0xffffffffu, (unsigned)min(nz[0] ? ex[0] : kNoExp,
+                                                                         nz[1] ? ex[1] : kNoExp));
+    const int emax = __reduce_max_sync(0xffffffffu, max(nz[0] ? ex[0] : -kNoExp,
+                                                        nz[1] ? ex[1] : -kNoExp));
+    long long part = 0;
+    if (!bad && emin != kNoExp && emax - emin <= 36) {
+      const int base_e = max(emin, 1);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (nz[h]) {
+          const int e_eff = max(ex[h], 1);
+          const long long m = (long long)(((u[h] >> 16) & 0x7Fu) | (ex[h] ? 0x80u : 0u));
+          const long long term = m << (e_eff - base_e);
+          part += (u[h] >> 31) ? -term : term;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    }
+    if (lane == 0) {
+      emin_s = emin;
+      emax_s = emax;
+      bad_s = bad;
+      part_s = part;
+    }
+  }
+  cluster.sync();
+  if (threadIdx.x == 0) {
+    int gmin = kNoExp, gmax = -kNoExp, gbad = 0;
+    int emin_r[kFinCluster];
+    long long part_r[kFinCluster];
+#pragma unroll
+    for (int r = 0; r < kFinCluster; ++r) {
+      emin_r[r] = *cluster.map_shared_rank(&emin_s, r);
+      part_r[r] = *cluster.map_shared_rank(&part_s, r);
+      gmin = min(gmin, emin_r[r]);
+      gmax = max(gmax, *cluster.map_shared_rank(&emax_s, r));
+      gbad |= *cluster.map_shared_rank(&bad_s, r);
+    }
+    double mu;
+    if (gbad == 0 && gmin == kNoExp) {
+      mu = 0.0;  // every q_j is zero
+    } else if (gbad == 0 && gmax - gmin <= 36) {
+      const int g_e = max(gmin, 1);
+      long long S = 0;
+#pragma unroll
+      for (int r = 0; r < kFinCluster; ++r)
+        if (emin_r[r] != kNoExp) S += part_r[r] << (max(emin_r[r], 1) - g_e);
+      // 2^(g_e - 134 - log2 E) as a double (a normal number for every g_e)
+      const double scale = __longlong_as_double((long long)(g_e - 134 - log2E + 1023) << 52);
+      mu = __dmul_rn((double)S, scale);
+    } else {
+      double sum = 0.0;
+      for (int r = 0; r < kFinCluster; ++r) {
+        const float* qr = cluster.map_shared_rank(q_s, r);
+        for (int jl = 0; jl < per; ++jl) sum = __dadd_rn(sum, (double)qr[jl]);
+      }
+      mu = __ddiv_rn(sum, (double)E);
+    }
+    mu_s = mu;
+  }
+  __syncthreads();
+  const double mu = mu_s;
+  for (int jl = threadIdx.x; jl < per; jl += kFinThreads)
+    bias_out[j0 + jl] = __double2float_rn(__dsub_rn((double)q_s[jl], mu));
+  cluster.sync();  // keep every CTA's shared memory alive until the others have read it
 }
 
 // ------------------------------------------------------------------------
@@ -380,11 +451,11 @@ int launch_zero_i32(int32_t* p, int64_t n, cudaStream_t stream) {
 
 int launch_finalize(int32_t* hist_hi, int32_t* hist_lo, const int32_t* sel, const int32_t* r_lo,
                     int E, float* bias_out, uint16_t* qkey_out, int reset, cudaStream_t stream) {
-  eqb_lo_select_kernel<<<E, 256, 0, stream>>>(hist_hi, hist_lo, sel, r_lo, bias_out, qkey_out,
-                                              reset);
-  int st = launch_status();
-  if (st != QB_OK) return st;
-  eqb_center_kernel<<<1, 512, 0, stream>>>(bias_out, E);
+  if (E % kFinCluster != 0 || E / kFinCluster > 64) return QB_EUNSUPPORTED;
+  int log2E = 0;
+  while ((1 << log2E) < E) ++log2E;  // E is a power of two
+  eqb_finalize_kernel<<<kFinCluster, kFinThreads, 0, stream>>>(hist_hi, hist_lo, sel, r_lo, E, log2E,
+                                                               bias_out, qkey_out, reset);
   return launch_status();
 }
 

@@ -241,3 +241,65 @@ def test_keys_hist_lo_equals_definition(qb, orc, E, N):
     qb.qb_keys_hist_lo(keys, sel, h)
     torch.cuda.synchronize()
     assert np.array_equal(h.cpu().numpy(), want)
+
+
+def _keys_of(values):
+    # order-preserving key of each bf16 number given as fp32 (+0 for -0)
+    v = np.asarray(values, np.float32).copy()
+    v[v == 0] = 0.0
+    b = (v.view(np.uint32) >> 16).astype(np.uint32)
+    return np.where(b & 0x8000, b ^ 0xFFFF, b ^ 0x8000).astype(np.uint16)
+
+
+@pytest.mark.parametrize("E", [32, 64, 128, 256, 512])
+@pytest.mark.parametrize("spread", ["narrow", "wide", "no_bin"])
+def test_finalize_on_built_histograms(qb, orc, E, spread):
+    # qb_finalize against the plain definition on hand-built histograms: the
+    # selected key of each expert is known, extra counts sit below and above
+    # it in its bin so that the rank lands mid-row, and the quantiles span a
+    # narrow exponent range (the tree sum is exact) or about 2^-60 .. 2^60
+    # (the serial ascending sum decides), or one expert has no selected bin
+    # (every output NaN, as the mean is undefined).  Keys at lo bytes 0x00
+    # and 0xFF are included.
+    rng = np.random.default_rng(E * 3 + len(spread))
+    if spread == "wide":
+        mag = 2.0 ** rng.integers(-60, 61, E)
+    else:
+        mag = 2.0 ** rng.integers(-3, 3, E)
+    vals = (rng.uniform(1, 2, E) * mag * rng.choice([-1.0, 1.0], E)).astype(np.float32)
+    vals = (vals.view(np.uint32) & 0xFFFF0000).view(np.float32)  # bf16 numbers
+    keys = _keys_of(vals)
+    keys[0] = (keys[0] & 0xFF00) | 0x00
+    keys[1] = (keys[1] & 0xFF00) | 0xFF
+    sel = (keys >> 8).astype(np.int32)
+    lo = (keys & 0xFF).astype(np.int32)
+    hist_lo = np.zeros((E, 256), np.int32)
+    r_lo = np.zeros(E, np.int32)
+    for j in range(E):
+        below = int(rng.integers(0, 5)) if lo[j] > 0 else 0
+        if below:
+            hist_lo[j, rng.integers(0, lo[j], below)] += 1
+        at = int(rng.integers(1, 4))
+        hist_lo[j, lo[j]] += at
+        if lo[j] < 255:
+            hist_lo[j, rng.integers(lo[j] + 1, 256, 3)] += 1
+        r_lo[j] = hist_lo[j, :lo[j]].sum() + int(rng.integers(1, at + 1))
+    if spread == "no_bin":
+        sel[E // 2] = -1
+    hist_hi = rng.integers(0, 9, (E, 256)).astype(np.int32)
+    d = {n: torch.from_numpy(a).cuda() for n, a in
+         (("hh", hist_hi), ("hl", hist_lo), ("sel", sel), ("rlo", r_lo))}
+    b_out = torch.empty(E, dtype=torch.float32, device="cuda")
+    qk = torch.empty(E, dtype=torch.int16, device="cuda")
+    qb.qb_finalize(d["hh"], d["hl"], d["sel"], d["rlo"], b_out, qkey_out=qk, reset=True)
+    torch.cuda.synchronize()
+    got = b_out.cpu().numpy()
+    assert int(d["hh"].abs().sum()) == 0 and int(d["hl"].abs().sum()) == 0
+    if spread == "no_bin":
+        assert np.isnan(got).all()
+        assert np_u16(qk)[E // 2] == 0
+        return
+    assert np.array_equal(np_u16(qk), keys)
+    q = orc.key_decode_array(keys).astype(np.float64)
+    want = orc.center(q)
+    assert np.array_equal(got.view(np.int32), want.view(np.int32))

@@ -48,17 +48,28 @@ ROUTE_SOURCES = ("qb_route.cuh", "qb_device.cuh", "qb_route_hi.cu")
 # Warp instructions of the same capture (smsp__inst_executed.sum), for the
 # issue-rate roofline of this issue-bound kernel; same hash guard.
 ROUTE_INSTR = {"tokens": 524288, "warp_instructions": 177414280}
+# Warp instructions (smsp__inst_executed.sum) of one K3 microbatch of 65536
+# bf16 tokens: the routing kernel in K3 mode plus the count kernel, from the
+# ncu capture summarised in profiles/k3_one_microbatch.md; reported while the
+# K3 sources hash to the value they had when it was taken.
+K3_INSTR = {"sha1": "a4ce8f5b660869349346fef6e33c411374a75b14", "tokens": 65536,
+            "warp_instructions": 24588544 + 7044848}
+K3_SOURCES = ("qb_route.cuh", "qb_device.cuh", "qb_route_k3.cu", "qb_k3.cu")
 UNIT = "tokens/s/layer"
 WORKLOAD = "full_step"
 
 
-def _route_sources_match() -> bool:
+def _sources_sha1(files) -> str:
     import hashlib
     h = hashlib.sha1()
-    for f in ROUTE_SOURCES:
+    for f in files:
         with open(os.path.join(ROOT, "exact_distributed_quantiles_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
-    return h.hexdigest() == ROUTE_TRAFFIC["sha1"]
+    return h.hexdigest()
+
+
+def _route_sources_match() -> bool:
+    return _sources_sha1(ROUTE_SOURCES) == ROUTE_TRAFFIC["sha1"]
 
 
 def _issue_peak():
@@ -314,7 +325,15 @@ def k3_component(qb, inputs, dev, reps, warmup, peak_hbm):
         "roofline": {"bound": "hbm", "kernel": "k3_route_hist (route_kernel K3 mode + k3_count)",
                      "achieved": k3_bytes / (ms_hist / 1e3) / 1e9, "peak": peak_hbm,
                      "unit": "GB/s", "frac": k3_bytes / (ms_hist / 1e3) / 1e9 / peak_hbm,
-                     "bytes_per_batch": k3_bytes, "hist_ms_per_batch": ms_hist}}
+                     "bytes_per_batch": k3_bytes, "hist_ms_per_batch": ms_hist},
+        # both K3 passes are bound by instruction issue, not by HBM
+        "roofline_issue": (None if K3_INSTR["warp_instructions"] is None
+                           or _sources_sha1(K3_SOURCES) != K3_INSTR["sha1"] else {
+            "bound": "alu", "kernel": "k3_route_hist (route_kernel K3 mode + k3_count)",
+            "achieved": K3_INSTR["warp_instructions"] * w3.n_pool / K3_INSTR["tokens"]
+            / (ms_hist / 1e3), "peak": _issue_peak(), "unit": "warp instructions/s",
+            "frac": K3_INSTR["warp_instructions"] * w3.n_pool / K3_INSTR["tokens"]
+            / (ms_hist / 1e3) / _issue_peak()})}
 
 
 def gemm_component(qb, inputs, dev, reps, warmup, peak_hbm, peaks):

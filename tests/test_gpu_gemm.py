@@ -129,3 +129,35 @@ def test_fused_epilogue_exact_path_on_ties(qb, orc):
     logits, res = _fused(qb, hidden, w_t, bias, k)
     ref = assert_route_matches(orc, res, logits.cpu().numpy(), bias.cpu().numpy(), k)
     assert np.array_equal(res["hist"], orc.hist_hi(orc.keys(ref["margins"])))
+
+
+def test_fused_counts_past_one_launch(qb):
+    # More tokens than one launch of the fused kernel covers (SMs x 511 tiles
+    # x 128 tokens): the call is split so that no CTA's 16-bit window counter
+    # sees 2^16 tokens.  The first half of the hidden rows are identical, so
+    # every token of a CTA there lands in the same bin of each expert and an
+    # overflowing counter would show; the counts and keys must equal those of
+    # the plain GEMM followed by the routing kernel (32-bit counters).
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    M, H, E, k = sms * 511 * 128 + 1037, 64, 256, 6
+    g = torch.Generator(device="cuda")
+    g.manual_seed(9)
+    hidden = torch.randn(1, H, generator=g, device="cuda").expand(M, H).contiguous()
+    hidden[M // 2:] = torch.randn(M - M // 2, H, generator=g, device="cuda")
+    hidden = hidden.to(torch.bfloat16)
+    w_t = (torch.randn(E, H, generator=g, device="cuda") * H ** -0.5).to(torch.bfloat16)
+    bias = (torch.rand(E, generator=g, device="cuda") * 2 - 1) * 0.1
+    hist_f = torch.zeros(E, 256, dtype=torch.int32, device="cuda")
+    keys_f = torch.empty(M, E, dtype=torch.int16, device="cuda")
+    qb.qb_router_gemm_hist_hi(hidden, w_t, bias, k, None, hist_f, keys_out=keys_f)
+    logits = torch.empty(M, E, dtype=torch.float32, device="cuda")
+    qb.qb_router_gemm(hidden, w_t, logits)
+    hist_r = torch.zeros_like(hist_f)
+    keys_r = torch.empty_like(keys_f)
+    qb.qb_route_hist_hi(logits, bias, k, hist_r, keys_out=keys_r)
+    torch.cuda.synchronize()
+    assert qb.device_status() == 0
+    assert int(hist_f.sum()) == M * E
+    assert int(hist_f.max()) >= 1 << 16  # some bin holds more than a 16-bit counter can
+    assert torch.equal(hist_f, hist_r)
+    assert torch.equal(keys_f, keys_r)

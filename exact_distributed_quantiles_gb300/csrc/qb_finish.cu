@@ -1,5 +1,6 @@
-// qb_finish.cu -- the EQB second pass from stored keys, the rank selects, the
-// bias finalizers (EQB and K3), and small utility kernels.
+// qb_finish.cu -- the EQB second pass from stored keys, the hi-byte select,
+// the EQB bias finalizer, rank-averaged QB, and small utility kernels (the
+// K3 finalizer is in qb_k3.cu).
 //
 // "Exact Quantile Balancing and Load-Error Injection for Mixture-of-Experts",
 //   EQB paragraph: locate the hi-byte bin holding the r-th smallest value,

@@ -8,13 +8,18 @@
 // Reading used here: rho_raw = (load_e - T)/T with T = n*k/E, and
 // rho = tanh(rho_raw) - mean_e tanh(rho_raw).
 //
-// Two kernels:
-//   lei_rho_kernel    one 8-CTA cluster per local batch: load counts in
-//                     shared memory, reduced over the cluster, rho in fp32,
-//                     c_e = eta * rho_e into the caller's workspace
-//                     [num_batches, E];
-//   lei_apply_kernel  grid-stride stream over grad in 16-byte chunks:
-//                     grad += c_e of the chunk's batch (c rows stay in L1/L2).
+// Kernels:
+//   lei_rho_kernel         one 8-CTA cluster per local batch: load counts in
+//                          shared memory, reduced over the cluster, rho in
+//                          fp32, c_e = eta * rho_e into the caller's
+//                          workspace [num_batches, E] (lei_rho);
+//   lei_apply_kernel       grad += c_e of the row's batch, streamed in 16-byte
+//                          chunks by small CTAs that each own a run of rows
+//                          (lei_apply, lei_inject);
+//   lei_apply_bulk_kernel  the same update done by the bulk-copy unit's
+//                          reductions into L2, one warp per SM, launched to
+//                          run beside the preceding kernel (lei_apply_overlap).
+//   load_count_kernel and maxvio_kernel (qb_maxvio) share the counting.
 #include <cooperative_groups.h>
 
 #include "qb_device.cuh"

@@ -232,8 +232,14 @@ def test_lei_apply_overlap_equals_apply(qb, N, E, bt):
     bt_eff = bt or N
     nb = (N + bt_eff - 1) // bt_eff
     ws = torch.randn(nb, E, generator=g, device="cuda") * 1e-5
+    # subnormal sums, signed zeros, exact cancellation and a large addend
+    grad[0, :8] = torch.tensor([1e-39, -1e-39, 3e-45, 0.0, -0.0, 1e30, -2.0, 5e-38], device="cuda")
+    ws[0, :8] = torch.tensor([0.0, 0.0, 0.0, -0.0, -0.0, 1.0, 2.0, -5e-38], device="cuda")
     want = grad.clone()
     qb.lei_apply(want, ws, batch_tokens=bt)
+    g0 = grad.cpu().numpy()
+    exact = (g0 + ws.cpu().numpy()[np.arange(N) // bt_eff]).astype(np.float32)
+    assert np.array_equal(want.cpu().numpy().view(np.int32), exact.view(np.int32))
     alone = grad.clone()
     qb.lei_apply_overlap(alone, ws, batch_tokens=bt)
     torch.cuda.synchronize()

@@ -303,3 +303,31 @@ def test_finalize_on_built_histograms(qb, orc, E, spread):
     q = orc.key_decode_array(keys).astype(np.float64)
     want = orc.center(q)
     assert np.array_equal(got.view(np.int32), want.view(np.int32))
+
+
+@pytest.mark.parametrize("E", [32, 64, 128, 256, 512])
+@pytest.mark.parametrize("k", [1, 6, 15])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_lo_pass_recomputed_all_shapes(qb, orc, E, k, dtype):
+    # The lo pass that recomputes the keys from the logits (qb_route_hist_lo)
+    # equals the oracle's direct count on its own keys, for every expert count
+    # (E = 512 reads the selected bins of two 256-expert halves), fp32 and
+    # bf16 logits and a ragged token count.  sel comes from the oracle's
+    # select, so both sides count the same bins.
+    if k >= E:
+        pytest.skip("k must be below E")
+    N = 32 * 9 + 21
+    x, b = _logits(N, E, seed=E * 31 + k + (dtype == torch.bfloat16),
+                   dtype=dtype, std=1.5 if dtype == torch.bfloat16 else 1.0)
+    ref = orc.route(host_logits(x), b.cpu().numpy(), k, want=("margins",))
+    keys = orc.keys(ref["margins"])
+    sel, _ = orc.select_hi(orc.hist_hi(keys), orc.rank(N, E, k))
+    sel = np.asarray(sel, np.int32).copy()
+    sel[::5] = -1  # experts without a selected bin count nothing
+    want = orc.hist_lo(keys, sel)
+    h = torch.zeros(E, 256, dtype=torch.int32, device="cuda")
+    qb.qb_route_hist_lo(x, b, k, torch.from_numpy(sel).cuda(), h)
+    torch.cuda.synchronize()
+    assert qb.device_status() == 0
+    assert np.array_equal(h.cpu().numpy(), want)
+    assert int(h.sum()) > 0

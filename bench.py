@@ -57,6 +57,7 @@ K3_INSTR = {"sha1": "a4ce8f5b660869349346fef6e33c411374a75b14", "tokens": 65536,
 K3_SOURCES = ("qb_route.cuh", "qb_device.cuh", "qb_route_k3.cu", "qb_k3.cu")
 UNIT = "tokens/s/layer"
 WORKLOAD = "full_step"
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal
 
 
 def _sources_sha1(files) -> str:
@@ -701,7 +702,11 @@ def main():
                 "eqb_achieved": eqb_bytes * fs.L / ((ms_eqb / args.steps) / 1e3) / 1e9,
                 "peak": peak, "unit": "GB/s",
                 "frac": step_bytes * fs.L / (ms_step / 1e3) / 1e9 / peak,
-                "eqb_frac": eqb_bytes * fs.L / ((ms_eqb / args.steps) / 1e3) / 1e9 / peak},
+                "eqb_frac": eqb_bytes * fs.L / ((ms_eqb / args.steps) / 1e3) / 1e9 / peak,
+                # the same against GB300's nominal HBM3e bandwidth (8 TB/s)
+                "frac_nominal": step_bytes * fs.L / (ms_step / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+                "eqb_frac_nominal": eqb_bytes * fs.L / ((ms_eqb / args.steps) / 1e3) / 1e9
+                / NOMINAL_HBM_GBS},
             "roofline": {"bound": "hbm", "kernel": "qb_route_hist_hi (route_kernel hi mode)",
                          "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                          "unit": "GB/s", "frac": achieved / peak, "traffic": _route_traffic(n),

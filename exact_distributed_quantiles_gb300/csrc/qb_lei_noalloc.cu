@@ -10,11 +10,14 @@
 // entry point keeps that scratch in a fixed-size array in the library's own
 // device memory instead and allocates nothing.
 //
-// The array is a file-scope __device__ variable: every GPU that loads the
-// library holds it (kScratchFloats * 4 bytes) until the process exits.  Its
-// name is only a host-side stand-in in host code, so the device address is
-// looked up with cudaGetSymbolAddress once per device, with that device
-// current, on the first call made on that device.
+// The array is a file-scope __device__ variable.  Its name is only a host-side
+// stand-in in host code, so the device address is looked up with
+// cudaGetSymbolAddress, with the device current, on the first successful call
+// made on that device.  Under CUDA's lazy module loading (the default) that
+// lookup is also what loads this library's device code on the device and
+// reserves the array (kScratchFloats * 4 bytes); under eager loading
+// (CUDA_MODULE_LOADING=EAGER) the reservation happens when the library's
+// context is set up.  Either way the array then stays until the process exits.
 #include <mutex>
 
 #include "qb_internal.h"
@@ -27,22 +30,25 @@ constexpr int64_t kScratchFloats = 65536;  // num_batches * E must not exceed th
 static __device__ __align__(256) float g_lei_scratch[kScratchFloats];
 
 constexpr int kMaxDevices = 64;
-struct ScratchSlot {
-  std::once_flag once;
-  float* ptr = nullptr;
-};
-ScratchSlot g_scratch[kMaxDevices];
+std::mutex g_scratch_mu;
+float* g_scratch[kMaxDevices] = {};
 
-// Device address of g_lei_scratch on the current device, or nullptr.
+// Device address of g_lei_scratch on the current device, or nullptr.  Only a
+// successful lookup is cached: after a failure (for instance a first call made
+// inside a stream capture) the error is cleared and the next call tries again.
 float* scratch_on_current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  ScratchSlot* s = &g_scratch[dev];
-  std::call_once(s->once, [s] {
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_lei_scratch) == cudaSuccess) s->ptr = static_cast<float*>(p);
-  });
-  return s->ptr;
+    if (cudaGetSymbolAddress(&p, g_lei_scratch) == cudaSuccess) {
+      g_scratch[dev] = static_cast<float*>(p);
+    } else {
+      (void)cudaGetLastError();
+    }
+  }
+  return g_scratch[dev];
 }
 
 }  // namespace

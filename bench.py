@@ -39,9 +39,9 @@ import torch  # noqa: E402
 METRIC = "QB routed tokens/s per layer (E=256,k=6, 2-pass EQB) on 1 GB300; % of HBM roofline"
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one route-kernel
-# launch on a 524288-token layer, from the ncu capture summarised in
-# profiles/route_kernel_hi_one_layer.md.  Reported only while the kernel's
-# sources hash to the value they had when the counters were taken.
+# launch on a 524288-token layer, from an ncu capture of that launch.  Reported
+# only while the kernel's sources hash to the value they had when the counters
+# were taken.
 ROUTE_TRAFFIC = {"sha1": "3e4d4f59d2ed626bde6df758fd648c9a4b198f25", "tokens": 524288,
                  "bytes": (537.009408 + 245.643264) * 1e6}
 ROUTE_SOURCES = ("qb_route.cuh", "qb_device.cuh", "qb_route_hi.cu")
@@ -49,9 +49,9 @@ ROUTE_SOURCES = ("qb_route.cuh", "qb_device.cuh", "qb_route_hi.cu")
 # issue-rate roofline of this issue-bound kernel; same hash guard.
 ROUTE_INSTR = {"tokens": 524288, "warp_instructions": 177414280}
 # Warp instructions (smsp__inst_executed.sum) of one K3 microbatch of 65536
-# bf16 tokens: the routing kernel in K3 mode plus the count kernel, from the
-# ncu capture summarised in profiles/k3_one_microbatch.md; reported while the
-# K3 sources hash to the value they had when it was taken.
+# bf16 tokens: the routing kernel in K3 mode plus the count kernel, from an
+# ncu capture of those launches; reported while the K3 sources hash to the
+# value they had when it was taken.
 K3_INSTR = {"sha1": "a4ce8f5b660869349346fef6e33c411374a75b14", "tokens": 65536,
             "warp_instructions": 24588544 + 7044848}
 K3_SOURCES = ("qb_route.cuh", "qb_device.cuh", "qb_route_k3.cu", "qb_k3.cu")
@@ -301,14 +301,14 @@ def k3_component(qb, inputs, dev, reps, warmup, peak_hbm):
     copies = [[m.clone() for m in mbs3] for _ in range(4)]
     bounds = inputs.k3_initial_bounds(bias3).to(dev)
     hist3 = torch.zeros(w3.E, 1000, dtype=torch.int32, device=dev)
-    ws3 = torch.empty(w3.n_tokens, w3.E, dtype=torch.int16, device=dev)
+    alpha3 = torch.empty(w3.n_tokens, dtype=torch.float32, device=dev)
     b3 = bias3.clone()
     R3 = qb.rank(w3.n_pool, w3.E, w3.k)
     it = [0]
 
     def k3_hist_only():
         for m in copies[it[0] % 4]:
-            qb.k3_route_hist(m, b3, w3.k, bounds, hist3, ws3)
+            qb.k3_route_hist(m, b3, w3.k, bounds, hist3, alpha3)
         it[0] += 1
 
     def k3_batch():
@@ -378,9 +378,16 @@ def gemm_component(qb, inputs, dev, reps, warmup, peak_hbm, peaks):
     tflops = flops / (ms_g / 1e3) / 1e12
     gbs = gbytes / (ms_g / 1e3) / 1e9
     peak_tc = peaks.get("bf16_tflops")
-    # the bound is whichever floor is higher: 205 FLOP per HBM byte here, below
-    # the ridge (peak TFLOP/s / peak GB/s, about 283), so HBM
-    hbm_bound = peak_tc is None or gbytes / (peak_hbm * 1e9) >= flops / (peak_tc * 1e12)
+    # the fused kernel the path runs (gemm_route_kernel): per microbatch it
+    # reads the hidden states and W^T and writes the uint16 keys (the logits
+    # stay in tensor memory), and does the GEMM's flops
+    f_flops = 2.0 * n * H * E
+    f_bytes = n * H * 2 + H * E * 2 + n * E * 2
+    f_tflops = f_flops / (ms_f / 1e3) / 1e12
+    f_gbs = f_bytes / (ms_f / 1e3) / 1e9
+    # its bound is whichever floor is higher: about 226 FLOP per HBM byte
+    # here, below the ridge (peak TFLOP/s / peak GB/s, about 283), so HBM
+    f_hbm_bound = peak_tc is None or f_bytes / (peak_hbm * 1e9) >= f_flops / (peak_tc * 1e12)
     return {
         "workload": "router_gemm: 4x32768 tokens, hidden 2048 bf16 x W [2048,256] bf16 on the "
                     "tensor cores with the EQB hi pass (k=6) in the GEMM epilogue, then select, "
@@ -388,16 +395,22 @@ def gemm_component(qb, inputs, dev, reps, warmup, peak_hbm, peaks):
         "value": w5.n_pool / (ms5 / 1e3), "unit": "tokens/s", "ms_per_batch": ms5,
         "launches_per_batch": w5.n_micro + 3,
         "fused_ms_per_microbatch": ms_f,
-        "roofline": {"bound": "hbm" if hbm_bound else "tensor",
-                     "kernel": "router_gemm_kernel (tcgen05, TMEM; logits written)",
-                     "achieved": gbs if hbm_bound else tflops,
-                     "peak": peak_hbm if hbm_bound else peak_tc,
-                     "unit": "GB/s" if hbm_bound else "TFLOP/s",
-                     "frac": gbs / peak_hbm if hbm_bound else tflops / peak_tc,
-                     "gemm_ms_per_batch": ms_g, "bytes_per_batch": gbytes,
-                     "flops_per_batch": flops, "tensor_tflops": tflops,
-                     "tensor_frac": tflops / peak_tc if peak_tc else None,
-                     "hbm_gbs": gbs, "hbm_frac": gbs / peak_hbm}}
+        "roofline": {"bound": "hbm" if f_hbm_bound else "tensor",
+                     "kernel": "gemm_route_kernel (tcgen05 GEMM + hi pass in the epilogue; "
+                               "keys written, logits kept in tensor memory)",
+                     "achieved": f_gbs if f_hbm_bound else f_tflops,
+                     "peak": peak_hbm if f_hbm_bound else peak_tc,
+                     "unit": "GB/s" if f_hbm_bound else "TFLOP/s",
+                     "frac": f_gbs / peak_hbm if f_hbm_bound else f_tflops / peak_tc,
+                     "bytes_per_microbatch": f_bytes, "flops_per_microbatch": f_flops,
+                     "tensor_tflops": f_tflops,
+                     "tensor_frac": f_tflops / peak_tc if peak_tc else None,
+                     "hbm_gbs": f_gbs, "hbm_frac": f_gbs / peak_hbm},
+        # the plain GEMM (logits written) for comparison
+        "plain_gemm": {"ms_per_batch": ms_g, "bytes_per_batch": gbytes, "flops_per_batch": flops,
+                       "tensor_tflops": tflops,
+                       "tensor_frac": tflops / peak_tc if peak_tc else None,
+                       "hbm_gbs": gbs, "hbm_frac": gbs / peak_hbm}}
 
 
 def rank_average_component(qb, inputs, dev, reps, warmup, peak_hbm):
@@ -468,10 +481,11 @@ def components(qb, inputs, dev, reps, warmup, peak_hbm, peaks):
             "maxvio": maxvio_component(qb, inputs, dev, reps, warmup)}
 
 
-def cpu_baseline_sample(n_tokens: int, layer: int = 0):
+def cpu_baseline_sample(n_tokens: int, layer: int = 0, threads: int | None = None):
     """Oracle on a bounded sample: n_tokens of one full-step layer through EQB
     (route by full sort, keys, hi/lo counts, exact select by sort, centering)
-    and LEI per 32768-token local batch.  Returns (seconds, tokens, cores)."""
+    and LEI per 32768-token local batch.  threads: OpenMP threads for the
+    oracle (None: all cores).  Returns (seconds, tokens, threads used)."""
     import oracle
     from exact_distributed_quantiles_gb300 import inputs
     oracle.build()
@@ -483,13 +497,20 @@ def cpu_baseline_sample(n_tokens: int, layer: int = 0):
     mbs_np = [m.numpy() for m in mbs]
     b_np = bias.numpy()
     g_np = grad.numpy()
-    t0 = time.perf_counter()
-    oracle.eqb_global_batch(mbs_np, b_np, ws.k)
-    for m in mbs_np:
-        t = oracle.route(m, b_np, ws.k, want=("topk",))["topk"]
-        oracle.lei(g_np, t, ws.eta)
-    dt = time.perf_counter() - t0
-    return dt, ws.n_pool, oracle.num_threads()
+    all_cores = oracle.num_threads()
+    if threads is not None:
+        oracle.set_num_threads(threads)
+    try:
+        used = oracle.num_threads()
+        t0 = time.perf_counter()
+        oracle.eqb_global_batch(mbs_np, b_np, ws.k)
+        for m in mbs_np:
+            t = oracle.route(m, b_np, ws.k, want=("topk",))["topk"]
+            oracle.lei(g_np, t, ws.eta)
+        dt = time.perf_counter() - t0
+    finally:
+        oracle.set_num_threads(all_cores)
+    return dt, ws.n_pool, used
 
 
 def run_reference(args):
@@ -531,6 +552,7 @@ def main():
     ap.add_argument("--layers", type=int, default=48)
     ap.add_argument("--ref-tokens", type=int, default=32768)
     ap.add_argument("--cpu-tokens", type=int, default=524288)
+    ap.add_argument("--cpu-tokens-single", type=int, default=65536)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-components", action="store_true")
@@ -673,10 +695,14 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         dt, nt, cores = cpu_baseline_sample(args.cpu_tokens)
+        dt1, nt1, _ = cpu_baseline_sample(args.cpu_tokens_single, threads=1)
         cpu = {"value": nt / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"{nt} tokens of full-step layer 0 through the oracle's EQB "
                          "(full-sort routing, keys, counts, sort select, centering) + LEI "
-                         f"({dt:.1f} s)"}
+                         f"({dt:.1f} s on {cores} threads)",
+               "single_thread": {"value": nt1 / dt1, "unit": UNIT, "cores": 1,
+                                 "sample": f"{nt1} tokens of the same layer, one thread "
+                                           f"({dt1:.1f} s)"}}
 
     if rank == 0:
         line = {

@@ -100,7 +100,17 @@ int64_t qb_rank(int64_t n_pool, int E, int k) {
 
 int qb_sigmoid(const float* x, float* s, int64_t n, void* stream) {
   if (n < 0 || (n > 0 && (!x || !s))) return QB_EINVAL;
-  return launch_sigmoid(x, s, n, as_stream(stream));
+  return launch_sigmoid(x, s, n, 0, as_stream(stream));
+}
+
+int qb_sigmoid_scalar(const float* x, float* s, int64_t n, void* stream) {
+  if (n < 0 || (n > 0 && (!x || !s))) return QB_EINVAL;
+  return launch_sigmoid(x, s, n, 1, as_stream(stream));
+}
+
+int qb_selftest_wait_timeout(int64_t polls, void* stream) {
+  if (polls < 1 || polls > (int64_t)1 << 24) return QB_EINVAL;
+  return launch_wait_timeout_selftest((uint32_t)polls, as_stream(stream));
 }
 
 int qb_zero_i32(int32_t* p, int64_t n, void* stream) {
@@ -160,19 +170,23 @@ int qb_finalize(int32_t* hist_hi, int32_t* hist_lo, const int32_t* sel, const in
 }
 
 int k3_route_hist(const void* logits, int dtype, const float* bias, int64_t N, int E, int k,
-                  const float* bounds, int nbins, int32_t* hist, uint16_t* bins_ws,
+                  const float* bounds, int nbins, int32_t* hist, float* alpha_out,
                   void* stream) {
   int st = check_route_args(logits, dtype, bias, N, E, k);
   if (st != QB_OK) return st;
-  if (!bounds || !hist || !bins_ws) return QB_EINVAL;
-  if (!aligned16(bins_ws)) return QB_EINVAL;
+  if (!bounds || !hist || !alpha_out) return QB_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(alpha_out) & 3u) != 0) return QB_EINVAL;
   if (nbins < 1 || nbins > 65536) return QB_EINVAL;
   if (N == 0) return QB_OK;
   cudaStream_t s = as_stream(stream);
-  st = launch_route_k3(logits, dtype, bias, N, E, k, nullptr, bins_ws, nullptr, nullptr, nullptr,
-                       bounds, nbins, s);
+  if (E == 256)
+    st = dtype == QB_F32 ? launch_route256_alpha_f32(logits, bias, N, k, alpha_out, s)
+                         : launch_route256_alpha_bf16(logits, bias, N, k, alpha_out, s);
+  else
+    st = launch_route_k3(logits, dtype, bias, N, E, k, nullptr, nullptr, nullptr, alpha_out,
+                         nullptr, bounds, nbins, s);
   if (st != QB_OK) return st;
-  return launch_k3_count(bins_ws, N, E, nbins, hist, s);
+  return launch_k3_count(logits, dtype, alpha_out, N, E, bounds, nbins, hist, s);
 }
 
 int k3_finalize(int32_t* hist, int E, int nbins, int64_t r, float* bounds, float* bias_out,

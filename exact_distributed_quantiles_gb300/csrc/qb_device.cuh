@@ -106,6 +106,11 @@ __device__ __forceinline__ f2_t f2_sub(f2_t a, f2_t b) {
   asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
+  f2_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 __device__ __forceinline__ f2_t f2_splat(float v) { return f2_pack(v, v); }
 
 // Hardware reciprocal estimate.  The .ftz form is the bare estimate; the
@@ -117,12 +122,21 @@ __device__ __forceinline__ float rcp_approx(float d) {
   return y;
 }
 
-// Pinned sigmoid of two inputs with |x| <= kFastAbsX.  The reciprocal is
-// RN(1/d) from the hardware estimate refined by one Newton step
-// y <- y + y*(1 - d*y) in fma form (Markstein's method).  That this equals
-// the correctly rounded reciprocal for every d this function can produce is
-// checked by running it on every binary32 input against the oracle.
-__device__ __forceinline__ f2_t sigmoid2_fast(f2_t X) {
+// -sigmoid of two inputs with |x| <= kFastAbsX, by the pinned sequence.
+//  * 2^n is built from t's bit pattern: t = 1.5*2^23 + n and
+//    (bits(1.5*2^23) << 23) == 0 mod 2^32, so bits(t)*2^23 + bits(1.0f) is
+//    the pattern of 2^n (|n| <= 124 here, so 2^n is normal);
+//  * d = fma(p, 2^n, 1) = RN(1 + e): e = p*2^n is exact (a power-of-two
+//    scaling of a normal number), so this is the sequence's RN(1 + RN(e));
+//  * the reciprocal RN(1/d) is the hardware estimate refined by one Newton
+//    step (Markstein's method), taken on -d so that the sign folds in:
+//    y' = est(1/(-d)) = -y, r = fma(d, y', 1) = RN(1 - d*y) and
+//    fma(r, y', y') = -RN(y + r*y).
+// That the result equals the correctly rounded reciprocal of the pinned d for
+// every input (and that the estimate is odd in its argument) is checked by
+// running qb_sigmoid, which uses this function, on every binary32 input
+// against the oracle.
+__device__ __forceinline__ f2_t neg_sigmoid2_fast(f2_t X) {
   const f2_t T = f2_fma(X, f2_splat(-kL2E), f2_splat(kMagic));
   const f2_t N = f2_sub(T, f2_splat(kMagic));
   f2_t W = f2_fma(N, f2_splat(kLn2Hi), X);
@@ -134,20 +148,21 @@ __device__ __forceinline__ f2_t sigmoid2_fast(f2_t X) {
   P = f2_fma(P, W, f2_splat(kC2));
   P = f2_fma(P, W, f2_splat(kC1));
   P = f2_fma(P, W, f2_splat(kC0));
-  float p0, p1, t0, t1;
-  f2_unpack(P, p0, p1);
+  float t0, t1;
   f2_unpack(T, t0, t1);
-  // t = 1.5*2^23 + n, and (bits(1.5*2^23) << 23) == 0 mod 2^32, so
-  // (bits(t) << 23) == n << 23: adding it to p's exponent multiplies by 2^n.
-  const float e0 = __uint_as_float(__float_as_uint(t0) * 0x800000u + __float_as_uint(p0));
-  const float e1 = __uint_as_float(__float_as_uint(t1) * 0x800000u + __float_as_uint(p1));
-  const f2_t D = f2_add(f2_pack(e0, e1), f2_splat(1.0f));
-  const f2_t ND = f2_sub(f2_splat(0.0f), D);
+  const float s0 = __uint_as_float(__float_as_uint(t0) * 0x800000u + 0x3F800000u);
+  const float s1 = __uint_as_float(__float_as_uint(t1) * 0x800000u + 0x3F800000u);
+  const f2_t D = f2_fma(P, f2_pack(s0, s1), f2_splat(1.0f));
   float d0, d1;
   f2_unpack(D, d0, d1);
-  const f2_t Y = f2_pack(rcp_approx(d0), rcp_approx(d1));
-  const f2_t R = f2_fma(ND, Y, f2_splat(1.0f));
-  return f2_fma(R, Y, Y);
+  const f2_t YN = f2_pack(rcp_approx(-d0), rcp_approx(-d1));
+  const f2_t R = f2_fma(D, YN, f2_splat(1.0f));
+  return f2_fma(R, YN, YN);
+}
+
+// sigmoid of two inputs with |x| <= kFastAbsX (the negation is exact).
+__device__ __forceinline__ f2_t sigmoid2_fast(f2_t X) {
+  return f2_sub(f2_splat(0.0f), neg_sigmoid2_fast(X));
 }
 
 __device__ __forceinline__ float max_abs8(const float (&x)[8]) {
@@ -247,10 +262,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait: gives up after ~2^24 polls (well over a second), records
-// kDevTimeout in the device status word and returns false.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* status) {
-  for (uint32_t it = 0; it < (1u << 24); ++it) {
+// Bounded wait: gives up after `polls` polls (by default 2^24, well over a
+// second), records kDevTimeout in the device status word and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* status,
+                                                  uint32_t polls = 1u << 24) {
+  for (uint32_t it = 0; it < polls; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if (it > 64) __nanosleep(64);
   }

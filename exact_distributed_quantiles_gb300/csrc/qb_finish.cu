@@ -399,15 +399,23 @@ __global__ void zero_i32_kernel(int32_t* __restrict__ p, int64_t n) {
 
 // The pinned sigmoid through the same code the routing kernels run: chunks
 // of 8 go through sigmoid8 (packed fast path when every |x| <= 86, the exact
-// scalar path otherwise); a tail shorter than 8 uses the scalar path.
-__global__ void sigmoid_kernel(const float* __restrict__ x, float* __restrict__ s, int64_t n) {
+// scalar path otherwise); a tail shorter than 8 uses the scalar path.  With
+// `scalar` set every element takes the exact scalar path, which the routing
+// kernels run for a whole warp-chunk as soon as one of its inputs is large.
+__global__ void sigmoid_kernel(const float* __restrict__ x, float* __restrict__ s, int64_t n,
+                               int scalar) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t n8 = n / 8;
   for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < n8; c += stride) {
     float xv[8], sv[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) xv[i] = x[8 * c + i];
-    sigmoid8(xv, sv);
+    if (scalar) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sv[i] = sigmoid_pinned(xv[i]);
+    } else {
+      sigmoid8(xv, sv);
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) s[8 * c + i] = sv[i];
   }
@@ -415,7 +423,27 @@ __global__ void sigmoid_kernel(const float* __restrict__ x, float* __restrict__ 
     s[i] = sigmoid_pinned(x[i]);
 }
 
+// The bounded-wait path on demand: one warp waits on an mbarrier that
+// nothing completes (no arrival, no copy issued against it) with a short poll
+// limit, so the wait gives up, sets kDevTimeout and the kernel returns.
+__global__ void wait_timeout_selftest_kernel(int* status, uint32_t polls) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  (void)mbar_wait_bounded(&bar, 0u, status, polls);
+}
+
 }  // namespace
+
+int launch_wait_timeout_selftest(uint32_t polls, cudaStream_t stream) {
+  int* status = device_status_ptr();
+  if (!status) return QB_ECUDA;
+  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(status, polls);
+  return launch_status();
+}
 
 int launch_keys_hist_lo(const uint16_t* keys, int64_t N, int E, const int32_t* sel,
                         int32_t* hist_lo, cudaStream_t stream) {
@@ -466,12 +494,12 @@ int launch_rank_average(const uint16_t* qkeys, int P, int E, float* bias_out,
   return launch_status();
 }
 
-int launch_sigmoid(const float* x, float* s, int64_t n, cudaStream_t stream) {
+int launch_sigmoid(const float* x, float* s, int64_t n, int scalar, cudaStream_t stream) {
   if (n <= 0) return QB_OK;
   int64_t grid = (n / 8 + 255) / 256 + 1;
   const int64_t gmax = (int64_t)sm_count() * 16;
   if (grid > gmax) grid = gmax;
-  sigmoid_kernel<<<(unsigned)grid, 256, 0, stream>>>(x, s, n);
+  sigmoid_kernel<<<(unsigned)grid, 256, 0, stream>>>(x, s, n, scalar);
   return launch_status();
 }
 

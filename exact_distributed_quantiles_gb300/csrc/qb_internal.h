@@ -34,6 +34,18 @@ int launch_route_lo(const void* logits, int dtype, const float* bias, int64_t N,
 int launch_route_k3(const void* logits, int dtype, const float* bias, int64_t N, int E, int k,
                     int32_t* hist, uint16_t* keys_out, int32_t* topk_out, float* alpha_out,
                     const int32_t* sel, const float* bounds, int nbins, cudaStream_t stream);
+// EQB hi pass specialised to E = 256 (qb_route256.cuh), per input type.
+int launch_route256_hi_f32(const void* logits, const float* bias, int64_t N, int k,
+                           int32_t* hist, uint16_t* keys_out, int32_t* topk_out,
+                           float* alpha_out, cudaStream_t stream);
+int launch_route256_hi_bf16(const void* logits, const float* bias, int64_t N, int k,
+                            int32_t* hist, uint16_t* keys_out, int32_t* topk_out,
+                            float* alpha_out, cudaStream_t stream);
+// alpha per token only (the first half of the K3 pass), E = 256.
+int launch_route256_alpha_f32(const void* logits, const float* bias, int64_t N, int k,
+                              float* alpha_out, cudaStream_t stream);
+int launch_route256_alpha_bf16(const void* logits, const float* bias, int64_t N, int k,
+                               float* alpha_out, cudaStream_t stream);
 int launch_keys_hist_lo(const uint16_t* keys, int64_t N, int E, const int32_t* sel,
                         int32_t* hist_lo, cudaStream_t stream);
 int launch_select_hi(const int32_t* hist_hi, int E, int64_t r, int32_t* sel, int32_t* r_lo,
@@ -42,9 +54,10 @@ int launch_finalize(int32_t* hist_hi, int32_t* hist_lo, const int32_t* sel, cons
                     int E, float* bias_out, uint16_t* qkey_out, int reset, cudaStream_t stream);
 int launch_k3_finalize(int32_t* hist, int E, int nbins, int64_t r, float* bounds,
                        float* bias_out, int reset, cudaStream_t stream);
-int launch_k3_count(const uint16_t* bins, int64_t N, int E, int nbins, int32_t* hist,
-                    cudaStream_t stream);
+int launch_k3_count(const void* logits, int dtype, const float* alpha, int64_t N, int E,
+                    const float* bounds, int nbins, int32_t* hist, cudaStream_t stream);
 int launch_zero_i32(int32_t* p, int64_t n, cudaStream_t stream);
+int launch_wait_timeout_selftest(uint32_t polls, cudaStream_t stream);
 int launch_router_gemm_route(const void* hidden, const void* w_t, int64_t M, int K, int k,
                              const float* bias, int32_t* hist, uint16_t* keys_out,
                              int32_t* topk_out, float* alpha_out, float* logits_out,
@@ -53,7 +66,7 @@ int launch_rank_average(const uint16_t* qkeys, int P, int E, float* bias_out,
                         cudaStream_t stream);
 int launch_maxvio(const int32_t* topk, int64_t N, int E, int k, int64_t batch_tokens,
                   int32_t* loads, double* out, cudaStream_t stream);
-int launch_sigmoid(const float* x, float* s, int64_t n, cudaStream_t stream);
+int launch_sigmoid(const float* x, float* s, int64_t n, int scalar, cudaStream_t stream);
 int launch_lei(float* grad, const int32_t* topk, int64_t N, int E, int k, float eta,
                int64_t batch_tokens, float* workspace, cudaStream_t stream);
 int launch_lei_rho(const int32_t* topk, int64_t N, int E, int k, float eta,

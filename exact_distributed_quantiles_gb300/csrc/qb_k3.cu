@@ -1,5 +1,5 @@
-// qb_k3.cu -- K3 histogram mode: counting the stored bin indices, and the
-// finalize (interpolated quantile, centering, next bounds).
+// qb_k3.cu -- K3 histogram mode: the counts, and the finalize (interpolated
+// quantile, centering, next bounds).
 //
 // "[Dev] Add global-batch quantile balancing", "Quantile estimator": a uniform
 // histogram of nbins (1000) bins per expert over [min(b) - 1, max(b) + 1]; the
@@ -8,13 +8,17 @@
 // follow it.  "Implementation": the counts accumulate over the microbatches
 // of a global batch in one persistent histogram that is reset in place.
 //
-// Counting.  The route pass in K3 mode stores one uint16 bin index per
-// (token, expert) in a caller workspace.  A [E, nbins] histogram (1 MB at
-// E = 256, nbins = 1000) does not fit in shared memory, so a CTA owns a
-// slice of EG experts over a range of tokens (EG x nbins int32 counters in
-// shared memory) and adds each non-zero counter to the global histogram once
-// at the end.  The flush costs one L2 atomic per non-zero counter per CTA, so
-// the grid is one CTA per SM: fewer, longer CTAs mean fewer flushed counters.
+// Counting.  A [E, nbins] histogram (1 MB at E = 256, nbins = 1000) does not
+// fit in one SM's shared memory, and spreading it over a cluster does not pay
+// on this GPU: shared-memory reductions into another CTA of the cluster ran
+// 23 times slower than into the CTA's own (52 against 1198 G/s over the whole
+// GPU), and global atomics per element are slower still.  So the routing pass
+// (first launch) stops after alpha, and this kernel -- a CTA per expert slice
+// and token range -- recomputes the scores of its slice from the logits (the
+// same pinned function, bit for bit), forms the margins and their bins and
+// counts them in shared memory.  The logits of a 65536-token microbatch
+// (32 MiB of bf16) are still in L2 from the first launch.  Non-zero counters
+// are added to the global histogram once per CTA.
 //
 // Finalize.  One cluster of 8 CTAs: a warp per expert finds the bin (blocks
 // of 128 bins, coalesced loads, a warp scan per block), the
@@ -22,6 +26,7 @@
 // through distributed shared memory in rank order, so every CTA derives the
 // same mean; min and max of the new bias go through the cluster the same way.
 #include <cooperative_groups.h>
+#include <cuda_bf16.h>
 
 #include "qb_device.cuh"
 #include "qb_internal.h"
@@ -33,90 +38,160 @@ namespace {
 
 constexpr int kCountThreads = 1024;
 constexpr int kCountSmemMax = 200 * 1024;
+constexpr int kEW = 32;  // experts per counting CTA
 
 // No "memory" clobber: the counters are read only after a __syncthreads.
-__device__ __forceinline__ void red_shared_u32(uint32_t addr, uint32_t v) {
-  asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(addr), "r"(v));
+__device__ __forceinline__ void red_shared_inc(uint32_t addr) {
+  asm volatile("red.shared.add.u32 [%0], 1;" ::"r"(addr));
 }
 
-// EG experts per CTA (8 or 16): EG / 8 lanes per row, each lane reads 8
-// consecutive indices (16 bytes) of its row.  Counter (e, b) sits at word
-// e * row_w + b, row_w odd so that equal bins of different experts fall in
-// different banks.
-template <int EG>
+// Eight logits of a row (fp32 or bf16) as fp32.
+__device__ __forceinline__ void load8x(const float* p, float (&x)[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ void load8x(const __nv_bfloat16* p, float (&x)[8]) {
+  const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// The K3 counts from the logits and alpha (written by the first launch).
+// A CTA owns a slice of kEW experts over a range of tokens; a lane takes 8
+// consecutive experts of a row (4 lanes per row, 8 rows per warp), recomputes
+// their pinned scores -- the routing pass's function, negated, bit for bit --
+// the margins r = alpha + sn (= alpha - s) and the bins
+//   idx = clamp(floor(RN(RN(r - lo) * scale)), 0, nbins - 1)
+// (a float-to-int conversion truncates, saturates and sends NaN to 0, so the
+// clamp covers t < 0, t >= nbins and NaN as the definition does), and counts
+// them in shared memory: kEW rows of `pitch` int32 (pitch odd, so that equal
+// bins of different experts fall in different banks).  GLOBAL: the slice
+// would not fit shared memory, so every count is a global atomic.  Non-zero
+// shared counters are added to the global histogram once at the end.
+template <typename T, bool GLOBAL>
 __global__ void __launch_bounds__(kCountThreads, 1)
-    k3_count_kernel(const uint16_t* __restrict__ bins, int64_t N, int E, int nbins, int row_w,
+    k3_count_kernel(const T* __restrict__ logits, const float* __restrict__ alpha, int64_t N,
+                    int E, const float* __restrict__ bounds, int nbins, int pitch,
                     int32_t* __restrict__ hist, int64_t rows_per_cta) {
-  extern __shared__ uint32_t h[];
-  constexpr int LPR = EG / 8;
-  constexpr int RPW = 32 / LPR;  // rows per warp per load
+  extern __shared__ int32_t h[];
   constexpr int kWarps = kCountThreads / 32;
-  constexpr int kU = 4;          // loads in flight per lane
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const int n_eg = E / EG;
+  const int n_eg = E / kEW;
   const int eg = blockIdx.x % n_eg;
   const int64_t r_begin = (int64_t)(blockIdx.x / n_eg) * rows_per_cta;
   int64_t r_end = r_begin + rows_per_cta;
   if (r_end > N) r_end = N;
-  const uint32_t last = (uint32_t)(nbins - 1);
-  const int chunk = lane % LPR;
-  const int rsub = lane / LPR;
-  for (int i = threadIdx.x; i < EG * row_w; i += kCountThreads) h[i] = 0;
-  const uint32_t hb = (uint32_t)__cvta_generic_to_shared(h);
-  uint32_t ebase[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) ebase[j] = hb + 4u * (uint32_t)((8 * chunk + j) * row_w);
+  if constexpr (!GLOBAL) {
+    for (int i = threadIdx.x; i < kEW * pitch; i += kCountThreads) h[i] = 0;
+  }
+  const float lo = bounds[0];
+  const float scale = __fdiv_rn((float)nbins, __fsub_rn(bounds[1], bounds[0]));
+  const int last = nbins - 1;
+  const int chunk = lane & 3;   // experts 8*chunk .. 8*chunk+7 of the slice
+  const int rsub = lane >> 2;   // row of the warp's 8
+  const int e0 = eg * kEW + 8 * chunk;
+  const uint32_t hb = (uint32_t)__cvta_generic_to_shared(h) + 4u * (uint32_t)(8 * chunk * pitch);
   __syncthreads();
 
-  const int64_t n_rows = r_end > r_begin ? r_end - r_begin : 0;
-  const uint16_t* base = bins + r_begin * E + eg * EG + 8 * chunk;
-  const int64_t stride = (int64_t)kWarps * RPW * kU;
-  int64_t r0 = (int64_t)warp * RPW * kU + rsub;
-  uint4 cur[kU];
-#pragma unroll
-  for (int q = 0; q < kU; ++q) {
-    const int64_t r = r0 + RPW * q;
-    cur[q] = r < n_rows ? __ldcs(reinterpret_cast<const uint4*>(base + r * E))
-                        : make_uint4(0u, 0u, 0u, 0u);
+  const f2_t LO = f2_splat(lo), SC = f2_splat(scale);
+  const T* base = logits + e0;
+  int64_t r = r_begin + warp * 8 + rsub;
+  const int64_t stride = (int64_t)kWarps * 8;
+  float x[8], a = 0.0f;
+  bool act = r < r_end;
+  if (act) {
+    load8x(base + r * E, x);
+    a = __ldg(alpha + r);
   }
-  for (; r0 < n_rows; r0 += stride) {
-    uint4 nxt[kU];
-#pragma unroll
-    for (int q = 0; q < kU; ++q) {
-      const int64_t r = r0 + stride + RPW * q;
-      nxt[q] = r < n_rows ? __ldcs(reinterpret_cast<const uint4*>(base + r * E))
-                          : make_uint4(0u, 0u, 0u, 0u);
+  while (__any_sync(0xffffffffu, act)) {
+    // next rows in flight while this one is counted
+    const int64_t rn = r + stride;
+    const bool actn = rn < r_end;
+    float xn[8], an = 0.0f;
+    if (actn) {
+      load8x(base + rn * E, xn);
+      an = __ldg(alpha + rn);
     }
+    if (!act) {
 #pragma unroll
-    for (int q = 0; q < kU; ++q) {
-      if (r0 + RPW * q < n_rows) {
-        const uint32_t w[4] = {cur[q].x, cur[q].y, cur[q].z, cur[q].w};
+      for (int i = 0; i < 8; ++i) x[i] = 0.0f;
+    }
+    float m = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {  // min() keeps a stray index inside the slice
-          red_shared_u32(ebase[2 * i] + 4u * min(w[i] & 0xFFFFu, last), 1u);
-          red_shared_u32(ebase[2 * i + 1] + 4u * min(w[i] >> 16, last), 1u);
-        }
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[i]));
+    float sn[8];
+    if (__all_sync(0xffffffffu, m <= kFastAbsX)) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        f2_unpack(neg_sigmoid2_fast(f2_pack(x[2 * i], x[2 * i + 1])), sn[2 * i], sn[2 * i + 1]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sn[i] = -sigmoid_pinned(x[i]);
+    }
+    const f2_t A = f2_splat(a);
+    int idx[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      // t = RN(RN(r - lo) * scale) with r = RN(alpha + sn)
+      const f2_t R = f2_add(A, f2_pack(sn[2 * i], sn[2 * i + 1]));
+      float t0, t1;
+      f2_unpack(f2_mul(f2_sub(R, LO), SC), t0, t1);
+      idx[2 * i] = min(max(__float2int_rz(t0), 0), last);
+      idx[2 * i + 1] = min(max(__float2int_rz(t1), 0), last);
+    }
+    if (act) {
+      if constexpr (GLOBAL) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) atomicAdd(hist + (int64_t)(e0 + i) * nbins + idx[i], 1);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) red_shared_inc(hb + 4u * (uint32_t)(i * pitch + idx[i]));
       }
-      cur[q] = nxt[q];
     }
+    r = rn;
+    act = actn;
+    a = an;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = xn[i];
   }
-  __syncthreads();
-  for (int i = threadIdx.x; i < EG * nbins; i += kCountThreads) {
-    const int el = i / nbins, b = i - el * nbins;
-    const uint32_t c = h[el * row_w + b];
-    if (c) atomicAdd(hist + (int64_t)(eg * EG + el) * nbins + b, (int)c);
+  if constexpr (!GLOBAL) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < kEW * nbins; i += kCountThreads) {
+      const int el = i / nbins, b = i - el * nbins;
+      const int c = h[el * pitch + b];
+      if (c) atomicAdd(hist + (int64_t)(eg * kEW + el) * nbins + b, c);
+    }
   }
 }
 
-// Bins too many for a shared slice of 8 experts: one global atomic per index.
-__global__ void k3_count_global_kernel(const uint16_t* __restrict__ bins, int64_t n_elem, int E,
-                                       int nbins, int32_t* __restrict__ hist) {
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_elem; i += stride) {
-    const int e = (int)(i % E);
-    atomicAdd(hist + (int64_t)e * nbins + min((int)bins[i], nbins - 1), 1);
+template <typename T, bool GLOBAL>
+int launch_count_t(const T* logits, const float* alpha, int64_t N, int E, const float* bounds,
+                   int nbins, int32_t* hist, cudaStream_t stream) {
+  const int pitch = nbins | 1;
+  const int smem = GLOBAL ? 0 : kEW * pitch * 4;
+  static int attr_bytes = 0;  // per instantiation; benign race (idempotent)
+  if (smem > attr_bytes) {
+    if (cudaFuncSetAttribute(k3_count_kernel<T, GLOBAL>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return launch_status();
+    attr_bytes = smem;
   }
+  const int n_eg = E / kEW;
+  int64_t n_tr = sm_count() / n_eg;
+  const int64_t max_tr = (N + 255) / 256;  // at least 256 rows per CTA
+  if (n_tr > max_tr) n_tr = max_tr;
+  if (n_tr < 1) n_tr = 1;
+  const int64_t rows_per_cta = (N + n_tr - 1) / n_tr;
+  k3_count_kernel<T, GLOBAL><<<(unsigned)(n_tr * n_eg), kCountThreads, smem, stream>>>(
+      logits, alpha, N, E, bounds, nbins, pitch, hist, rows_per_cta);
+  return launch_status();
 }
 
 // ---- finalize -------------------------------------------------------------
@@ -273,41 +348,19 @@ __global__ void __cluster_dims__(kFinCluster, 1, 1) __launch_bounds__(kFinThread
   cluster.sync();  // keep every CTA's shared memory alive until rank 0 has read it
 }
 
-template <int EG>
-int launch_count(const uint16_t* bins, int64_t N, int E, int nbins, int row_w, int32_t* hist,
-                 cudaStream_t stream) {
-  const int smem = EG * row_w * 4;
-  static int attr_bytes = 0;  // per instantiation; benign race (idempotent)
-  if (smem > attr_bytes) {
-    if (cudaFuncSetAttribute(k3_count_kernel<EG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess)
-      return launch_status();
-    attr_bytes = smem;
-  }
-  const int n_eg = E / EG;
-  int64_t n_tr = sm_count() / n_eg;
-  const int64_t max_tr = (N + 255) / 256;  // at least 256 rows per CTA
-  if (n_tr > max_tr) n_tr = max_tr;
-  if (n_tr < 1) n_tr = 1;
-  const int64_t rows_per_cta = (N + n_tr - 1) / n_tr;
-  k3_count_kernel<EG><<<(unsigned)(n_tr * n_eg), kCountThreads, smem, stream>>>(
-      bins, N, E, nbins, row_w, hist, rows_per_cta);
-  return launch_status();
-}
-
 }  // namespace
 
-int launch_k3_count(const uint16_t* bins, int64_t N, int E, int nbins, int32_t* hist,
-                    cudaStream_t stream) {
-  const int row_w = nbins | 1;
-  if (16 * row_w * 4 <= kCountSmemMax) return launch_count<16>(bins, N, E, nbins, row_w, hist, stream);
-  if (8 * row_w * 4 <= kCountSmemMax) return launch_count<8>(bins, N, E, nbins, row_w, hist, stream);
-  const int64_t n_elem = N * E;
-  int64_t grid = (n_elem + 255) / 256;
-  const int64_t gmax = (int64_t)sm_count() * 8;
-  if (grid > gmax) grid = gmax;
-  k3_count_global_kernel<<<(unsigned)grid, 256, 0, stream>>>(bins, n_elem, E, nbins, hist);
-  return launch_status();
+int launch_k3_count(const void* logits, int dtype, const float* alpha, int64_t N, int E,
+                    const float* bounds, int nbins, int32_t* hist, cudaStream_t stream) {
+  const bool fits = kEW * (nbins | 1) * 4 <= kCountSmemMax;
+  if (dtype == QB_F32) {
+    const float* x = static_cast<const float*>(logits);
+    return fits ? launch_count_t<float, false>(x, alpha, N, E, bounds, nbins, hist, stream)
+                : launch_count_t<float, true>(x, alpha, N, E, bounds, nbins, hist, stream);
+  }
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(logits);
+  return fits ? launch_count_t<__nv_bfloat16, false>(x, alpha, N, E, bounds, nbins, hist, stream)
+              : launch_count_t<__nv_bfloat16, true>(x, alpha, N, E, bounds, nbins, hist, stream);
 }
 
 int launch_k3_finalize(int32_t* hist, int E, int nbins, int64_t r, float* bounds, float* bias_out,

@@ -1,7 +1,8 @@
 // qb_route.cuh -- the fused router pass (sigmoid, top-(k+1), margins, keys,
 // histograms) shared by the EQB hi pass, the recomputing EQB lo pass and the
-// K3 pass.  Included by qb_route_hi.cu, qb_route_lo.cu and qb_route_k3.cu,
-// each of which instantiates one mode.
+// K3 pass (which stops after alpha; qb_k3.cu counts).  Included by
+// qb_route_hi.cu, qb_route_lo.cu and qb_route_k3.cu, each of which
+// instantiates one mode; E = 256 routes through qb_route256.cuh instead.
 //
 // "[Dev] Add global-batch quantile balancing", "Quantile estimator":
 //   s = sigmoid(logit), alpha[i] = (k+1)-th largest of s[i,:] + b,
@@ -368,13 +369,6 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
   // shared byte address of this lane's counter for element i, slot 0
   const int copy = (E >= 256) ? 0 : (8 * lane) / E;
   const uint32_t hbase = smem_u32(hist_s) + 4u * (uint32_t)(copy * GE::CSTRIDE + (lane % GE::LPR));
-  float k3_lo = 0.f, k3_scale = 0.f, k3_nb = 0.f;
-  if constexpr (MODE == kModeK3) {
-    k3_lo = a.bounds[0];
-    const float w = __fsub_rn(a.bounds[1], a.bounds[0]);
-    k3_nb = (float)a.nbins;
-    k3_scale = __fdiv_rn(k3_nb, w);
-  }
 
   const int64_t n_tiles = (a.N + TILE - 1) / TILE;
   const int64_t wstride = (int64_t)gridDim.x * NW;
@@ -680,26 +674,11 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
       const bool act = row < rows;
       const int64_t tok = t0 + row;
       if constexpr (MODE == kModeK3) {
-        if (act) {
-          float s[8];
-          load8(sc + f, s);
-          const float alpha = alpha_s[row];
-          uint32_t bw[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float r = __fsub_rn(alpha, s[i]);
-            const float tt = __fmul_rn(__fsub_rn(r, k3_lo), k3_scale);
-            uint32_t idx;
-            if (!(tt >= 0.0f))
-              idx = 0u;
-            else if (tt >= k3_nb)
-              idx = (uint32_t)(a.nbins - 1);
-            else
-              idx = (uint32_t)__float2int_rz(tt);
-            bw[i >> 1] |= idx << ((i & 1) * 16);
-          }
-          *reinterpret_cast<uint4*>(a.keys_out + tok * E + e0) = make_uint4(bw[0], bw[1], bw[2], bw[3]);
-        }
+        // alpha only (phase B wrote it): the K3 counts are taken by the
+        // counting kernel from the logits and alpha
+        (void)tok;
+        (void)e0;
+        (void)act;
       } else {
         uint32_t kw[4] = {0u, 0u, 0u, 0u};
         bool out_of_window = false;

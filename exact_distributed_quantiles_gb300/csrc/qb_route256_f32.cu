@@ -1,0 +1,15 @@
+// qb_route256_f32.cu -- instantiates the E = 256 router pass for float logits
+// (a translation unit of its own so that the variants compile in parallel).
+#include "qb_route256.cuh"
+
+namespace qb {
+int launch_route256_hi_f32(const void* logits, const float* bias, int64_t N, int k,
+                            int32_t* hist, uint16_t* keys_out, int32_t* topk_out,
+                            float* alpha_out, cudaStream_t stream) {
+  return r256::launch_hi_t<float>(logits, bias, N, k, hist, keys_out, topk_out, alpha_out, stream);
+}
+int launch_route256_alpha_f32(const void* logits, const float* bias, int64_t N, int k,
+                               float* alpha_out, cudaStream_t stream) {
+  return r256::launch_alpha_t<float>(logits, bias, N, k, alpha_out, stream);
+}
+}  // namespace qb

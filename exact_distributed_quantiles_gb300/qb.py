@@ -19,12 +19,13 @@ LIB_PATH = os.path.join(_HERE, "libqb.so")
 QB_OK, QB_EINVAL, QB_EUNSUPPORTED, QB_ECUDA, QB_EOVERFLOW, QB_EDEVICE = 0, -1, -2, -3, -4, -5
 QB_F32, QB_BF16 = 0, 1
 
-EXPORTS = ("qb_status_string", "qb_version", "qb_rank", "qb_sigmoid", "qb_zero_i32",
+EXPORTS = ("qb_status_string", "qb_version", "qb_rank", "qb_sigmoid", "qb_sigmoid_scalar",
+           "qb_zero_i32",
            "qb_route_hist_hi", "qb_select_hi", "qb_keys_hist_lo", "qb_route_hist_lo",
            "qb_finalize", "k3_route_hist", "k3_finalize", "lei_inject", "qb_device_status",
            "lei_inject_noalloc", "qb_router_gemm", "qb_router_gemm_hist_hi", "qb_rank_average",
            "qb_maxvio", "lei_rho", "lei_apply",
-           "lei_apply_overlap")
+           "lei_apply_overlap", "qb_selftest_wait_timeout")
 
 
 class QBError(RuntimeError):
@@ -44,6 +45,7 @@ def _load():
         "qb_version": (ctypes.c_char_p, []),
         "qb_rank": (I64, [I64, I, I]),
         "qb_sigmoid": (I, [P, P, I64, P]),
+        "qb_sigmoid_scalar": (I, [P, P, I64, P]),
         "qb_zero_i32": (I, [P, I64, P]),
         "qb_route_hist_hi": (I, [P, I, P, I64, I, I, P, P, P, P, P]),
         "qb_select_hi": (I, [P, I, I64, P, P, P]),
@@ -62,6 +64,7 @@ def _load():
         "lei_rho": (I, [P, I64, I, I, F, I64, P, P]),
         "lei_apply": (I, [P, I64, I, I64, P, P]),
         "lei_apply_overlap": (I, [P, I64, I, I64, P, P]),
+        "qb_selftest_wait_timeout": (I, [I64, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -121,6 +124,10 @@ def qb_sigmoid(x, s, stream=None):
     _check("qb_sigmoid", lib.qb_sigmoid(_ptr(x), _ptr(s), x.numel(), _stream(stream)))
 
 
+def qb_sigmoid_scalar(x, s, stream=None):
+    _check("qb_sigmoid_scalar", lib.qb_sigmoid_scalar(_ptr(x), _ptr(s), x.numel(), _stream(stream)))
+
+
 def qb_zero_i32(t, stream=None):
     _check("qb_zero_i32", lib.qb_zero_i32(_ptr(t), t.numel(), _stream(stream)))
 
@@ -160,12 +167,12 @@ def qb_finalize(hist_hi, hist_lo, sel, r_lo, bias_out, qkey_out=None, reset=True
                            _ptr(qkey_out), 1 if reset else 0, _stream(stream)))
 
 
-def k3_route_hist(logits, bias, k, bounds, hist, bins_ws, stream=None):
+def k3_route_hist(logits, bias, k, bounds, hist, alpha_out, stream=None):
     N, E = logits.shape
     nbins = hist.shape[1]
     _check("k3_route_hist",
            lib.k3_route_hist(_ptr(logits), _dtype(logits), _ptr(bias), N, E, int(k), _ptr(bounds),
-                             nbins, _ptr(hist), _ptr(bins_ws), _stream(stream)))
+                             nbins, _ptr(hist), _ptr(alpha_out), _stream(stream)))
 
 
 def k3_finalize(hist, r, bounds, bias_out, reset=True, stream=None):

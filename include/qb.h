@@ -79,6 +79,13 @@ int64_t qb_rank(int64_t n_pool, int E, int k);
  * may alias. */
 int qb_sigmoid(const float* x, float* s, int64_t n, void* stream);
 
+/* The same function through the routing kernels' exact scalar sequence only
+ * (the packed fast path covers |x| <= 86; the kernels switch a whole chunk
+ * to this sequence when any input of it is larger).  Results equal
+ * qb_sigmoid's bit for bit; a diagnostic for checking both sequences.
+ * x, s: device fp32 [n]; may alias. */
+int qb_sigmoid_scalar(const float* x, float* s, int64_t n, void* stream);
+
 /* Fill n int32 values with zero (a convenience for histograms). */
 int qb_zero_i32(int32_t* p, int64_t n, void* stream);
 
@@ -145,16 +152,16 @@ int qb_finalize(int32_t* hist_hi, int32_t* hist_lo, const int32_t* sel, const in
  *   w = RN(hi - lo), scale = RN(nbins / w),
  *   idx = floor(RN(RN(r - lo) * scale)), clamped to [0, nbins-1],
  *   hist[j][idx] += 1, with r the fp32 margin.
- *   bounds  device fp32 [2] = {lo, hi}, lo < hi (read on the device).
- *   hist    device int32 [E, nbins]; 1 <= nbins <= 65536.
- *   bins_ws device uint16 [N, E] scratch owned by the caller, 16-byte
- *           aligned: the routing pass stores every idx there and a second
- *           kernel counts them (the histogram is too large to privatise per
- *           CTA whole).  Its contents afterwards are the bin indices.
- * Two launches on `stream`; the workspace must not be shared by calls that
- * may run concurrently. */
+ *   bounds    device fp32 [2] = {lo, hi}, lo < hi (read on the device).
+ *   hist      device int32 [E, nbins]; 1 <= nbins <= 65536.
+ *   alpha_out device fp32 [N]: receives alpha of every token.  The first of
+ *             the call's two launches routes the tokens and writes alpha
+ *             there; the second recomputes each expert slice's scores from
+ *             the logits and counts the margins' bins (a 1000-bin histogram
+ *             per expert is too large to count in one routing pass).
+ * Two launches on `stream`. */
 int k3_route_hist(const void* logits, int dtype, const float* bias, int64_t N, int E, int k,
-                  const float* bounds, int nbins, int32_t* hist, uint16_t* bins_ws,
+                  const float* bounds, int nbins, int32_t* hist, float* alpha_out,
                   void* stream);
 
 /* K3 quantile, centering and next bounds ([QB-PR] "Quantile estimator"):
@@ -262,16 +269,21 @@ int qb_router_gemm_hist_hi(const void* hidden, const void* w_t, int64_t M, int H
  * at start-up, or call sites that hold no allocator.
  * Same arguments and results as lei_inject, minus `workspace`: the eta*rho
  * scratch lives in a fixed array inside the library's device memory
- * (65536 floats = 256 KiB per GPU that loads the library, held until process
- * exit).  Requires ceil(N / batch_tokens) * E <= 65536, else returns
- * QB_EINVAL before launching anything.  Allocates nothing (no cudaMalloc or
- * cudaFree).  The first call on a device looks up the array's device address
- * on that device (cudaGetSymbolAddress); make that first call before any
- * stream capture.  All calls share the one array, which keeps the last call's
- * contents (every value read is first written by the same call, so nothing
- * needs clearing); calls that overlap on the GPU -- on different streams, or
- * from different host threads -- race on it and must be serialised by the
- * caller. */
+ * (65536 floats = 256 KiB per GPU, held until process exit).  Requires
+ * ceil(N / batch_tokens) * E <= 65536, else returns QB_EINVAL before
+ * launching anything.  Allocates nothing itself (no cudaMalloc or cudaFree).
+ * The first successful call on a device looks up the array's device address
+ * there (cudaGetSymbolAddress).  Under CUDA's default lazy module loading that
+ * lookup is also when the driver loads the library's device code on that
+ * device and reserves the 256 KiB (with CUDA_MODULE_LOADING=EAGER it happens
+ * when the context is created), so a caller with a fixed memory budget should
+ * make one call at start-up, and that first call must come before any stream
+ * capture.  A failed lookup returns QB_ECUDA, clears the CUDA error it left
+ * and is retried by the next call.  All calls share the one array, which
+ * keeps the last call's contents (every value read is first written by the
+ * same call, so nothing needs clearing); calls that overlap on the GPU -- on
+ * different streams, or from different host threads -- race on it and must
+ * be serialised by the caller. */
 int lei_inject_noalloc(float* grad, const int32_t* topk_idx, int64_t N, int E, int k, float eta,
                        int64_t batch_tokens, void* stream);
 
@@ -306,6 +318,15 @@ int qb_maxvio(const int32_t* topk_idx, int64_t N, int E, int k, int64_t batch_to
  * trapping (bit 0: a bounded wait timed out).  Synchronous; returns QB_OK
  * when clear, QB_EDEVICE when a flag was set, QB_ECUDA on a CUDA error. */
 int qb_device_status(int* flags_out);
+
+/* Diagnostic for the bounded-wait path of every kernel: launches one warp
+ * that waits on a shared-memory mbarrier nothing will complete (no arrival,
+ * no copy issued against it) with a limit of `polls` polls (1 <= polls <=
+ * 2^24).  The wait gives up, sets bit 0 of the device status word and the
+ * kernel returns, leaving no copy in flight; qb_device_status then reports
+ * QB_EDEVICE once.  The pages have no counterpart: it exists so that the
+ * status reporting can be tested without a GPU fault. */
+int qb_selftest_wait_timeout(int64_t polls, void* stream);
 
 #ifdef __cplusplus
 }

@@ -95,7 +95,8 @@ def test_argument_errors_are_reported_before_launch(lib):
     assert L.k3_route_hist(fake, 1, fake, 10, 256, 8, fake, 0, fake, fake, N0) == lib.QB_EINVAL
     assert L.k3_route_hist(fake, 1, fake, 10, 256, 8, N0, 1000, fake, fake, N0) == lib.QB_EINVAL
     assert L.k3_route_hist(fake, 1, fake, 10, 256, 8, fake, 1000, fake, N0, N0) == lib.QB_EINVAL
-    assert L.k3_route_hist(fake, 1, fake, 10, 256, 8, fake, 1000, fake, odd, N0) == lib.QB_EINVAL
+    assert L.k3_route_hist(fake, 1, fake, 10, 256, 8, fake, 1000, fake,
+                           ctypes.c_void_p(65537), N0) == lib.QB_EINVAL  # alpha_out misaligned
     assert L.k3_finalize(fake, 256, 1000, 0, fake, fake, 1, N0) == lib.QB_EINVAL
     assert L.k3_finalize(fake, 256, 70000, 5, fake, fake, 1, N0) == lib.QB_EINVAL
     # LEI

@@ -188,17 +188,21 @@ def test_reset_in_place_and_replay_counted_once(qb, orc):
     assert np.array_equal(st.hist_hi.cpu().numpy(), once)
 
 
-def test_full_step_layer_at_bench_size(qb, orc):
-    # One layer of the full-step workload in the launch configuration the
-    # benchmark times (all 16 microbatches of the layer in one hi-pass call),
-    # compared with the oracle over every token.
+@pytest.mark.parametrize("layer", [0, 23, 47])
+def test_full_step_layer_at_bench_size(qb, orc, layer):
+    # Layers 0, 23 and 47 of the full-step workload (their own seeds), each
+    # routed in both launch shapes: the 16 microbatch calls of 32768 tokens
+    # that the benchmark times, and one call over the whole layer.  Compared
+    # with the oracle over every token.
     w = inputs.WORKLOADS["full_step"]
     out = torch.empty(w.n_pool, w.E, dtype=torch.float32, device="cuda")
-    bias, mbs = inputs.router_layer(w, inputs.seed_for("full_step", 0), device="cuda", out=out)
-    res = _eqb_gpu(qb, [out], bias, w.k)
+    bias, mbs = inputs.router_layer(w, inputs.seed_for("full_step", layer), device="cuda",
+                                    out=out)
     ref = orc.eqb_global_batch([out.cpu().numpy()], bias.cpu().numpy(), w.k)
-    _check_eqb(res, ref)
-    assert np.array_equal(np_u16(res["keys"]), np.concatenate(ref["keys"]))
+    for parts in (mbs, [out]):
+        res = _eqb_gpu(qb, parts, bias, w.k)
+        _check_eqb(res, ref)
+        assert np.array_equal(np_u16(res["keys"]), np.concatenate(ref["keys"]))
 
 
 @pytest.mark.parametrize("E,k", [(32, 1), (64, 6), (128, 8), (256, 6), (512, 15)])

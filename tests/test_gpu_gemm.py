@@ -161,3 +161,41 @@ def test_fused_counts_past_one_launch(qb):
     assert int(hist_f.max()) >= 1 << 16  # some bin holds more than a 16-bit counter can
     assert torch.equal(hist_f, hist_r)
     assert torch.equal(keys_f, keys_r)
+
+
+def test_router_gemm_global_batch_chain(qb, orc):
+    # The router-GEMM workload end to end: four 32768-token microbatches of
+    # the fused GEMM + hi pass (logits kept in tensor memory), then select,
+    # the lo pass over the stored keys and the finalize.  Histograms, selected
+    # bins and keys, and the new bias are compared bit for bit with the oracle
+    # fed the plain GEMM's fp32 logits, which equal the fused kernel's bit for
+    # bit (test_fused_epilogue_matches_routing_of_its_logits).
+    w = inputs.WORKLOADS["router_gemm"]
+    bias, W, hs = inputs.gemm_layer(w, inputs.seed_for("router_gemm"), device="cuda")
+    w_t = W.t().contiguous()
+    n, E = w.n_tokens, w.E
+    st = qb.EQBState(E, "cuda")
+    keys = torch.empty(w.n_pool, E, dtype=torch.int16, device="cuda")
+    for i, h in enumerate(hs):
+        qb.qb_router_gemm_hist_hi(h, w_t, bias, w.k, None, st.hist_hi,
+                                  keys_out=keys[i * n:(i + 1) * n])
+    hist_hi = st.hist_hi.clone()
+    qb.qb_select_hi(st.hist_hi, qb.rank(w.n_pool, E, w.k), st.sel, st.r_lo)
+    qb.qb_keys_hist_lo(keys, st.sel, st.hist_lo)
+    hist_lo = st.hist_lo.clone()
+    b_out = torch.empty_like(bias)
+    qb.qb_finalize(st.hist_hi, st.hist_lo, st.sel, st.r_lo, b_out, qkey_out=st.qkey, reset=True)
+    logits = []
+    for h in hs:
+        lg = torch.empty(n, E, dtype=torch.float32, device="cuda")
+        qb.qb_router_gemm(h, w_t, lg)
+        logits.append(lg)
+    torch.cuda.synchronize()
+    assert qb.device_status() == 0
+    ref = orc.eqb_global_batch([lg.cpu().numpy() for lg in logits], bias.cpu().numpy(), w.k)
+    assert np.array_equal(hist_hi.cpu().numpy(), ref["hist_hi"])
+    assert np.array_equal(hist_lo.cpu().numpy(), ref["hist_lo"])
+    assert np.array_equal(st.sel.cpu().numpy(), ref["sel"])
+    assert np.array_equal(st.qkey.cpu().numpy().view(np.uint16), ref["qkey"])
+    assert np.array_equal(b_out.cpu().numpy().view(np.uint32), ref["bias_out"].view(np.uint32))
+    assert int(st.hist_hi.abs().sum()) == 0 and int(st.hist_lo.abs().sum()) == 0  # reset

@@ -38,21 +38,28 @@ def qb():
 
 def test_sigmoid_bit_equal_on_every_binary32_input(qb, orc):
     chunk = 1 << 28
+    # both device sequences: the packed fast path (with its per-chunk switch
+    # to the scalar one for large inputs) and the scalar one on every input
     x = torch.empty(chunk, dtype=torch.float32, device="cuda")
     s = torch.empty_like(x)
+    s1 = torch.empty_like(x)
     base = torch.arange(chunk, dtype=torch.int64, device="cuda")
-    mism = 0
+    mism = mism_scalar = 0
     for c in range(1 << 4):
         bits = (base + c * chunk).to(torch.int64)
         bits = torch.where(bits >= (1 << 31), bits - (1 << 32), bits).to(torch.int32)
         x.copy_(bits.view(torch.float32))
         qb.qb_sigmoid(x, s)
+        qb.qb_sigmoid_scalar(x, s1)
         xs = x.cpu().numpy()
         got = s.cpu().numpy().view(np.uint32)
+        got1 = s1.cpu().numpy().view(np.uint32)
         want = orc.sigmoid(xs).view(np.uint32)
         fin = ~np.isnan(xs)
         mism += int(np.count_nonzero(got[fin] != want[fin]))
+        mism_scalar += int(np.count_nonzero(got1[fin] != want[fin]))
     assert mism == 0
+    assert mism_scalar == 0
 
 
 # ------------------------------------------------------------------ K3
@@ -61,9 +68,9 @@ def _k3_gpu(qb, mbs, bias, k, bounds0, nbins):
     E = bias.shape[0]
     hist = torch.zeros(E, nbins, dtype=torch.int32, device="cuda")
     bounds = bounds0.clone().cuda()
-    ws = torch.empty(max(m.shape[0] for m in mbs), E, dtype=torch.int16, device="cuda")
+    alpha = torch.empty(max(m.shape[0] for m in mbs), dtype=torch.float32, device="cuda")
     for m in mbs:
-        qb.k3_route_hist(m, bias, k, bounds, hist, ws[:m.shape[0]])
+        qb.k3_route_hist(m, bias, k, bounds, hist, alpha[:m.shape[0]])
     n_pool = sum(m.shape[0] for m in mbs)
     h = hist.clone()
     b_out = torch.empty_like(bias)

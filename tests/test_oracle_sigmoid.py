@@ -110,9 +110,11 @@ def test_sigmoid_monotone_within_one_ulp(orc):
     x = np.sort(np.concatenate([np.linspace(-110, 110, 1_000_001, dtype=np.float32),
                                 np.arange(-1.0, 1.0, 2.0 ** -22, dtype=np.float32)]))
     s = orc.sigmoid(x)
-    # Non-decreasing up to one ulp: for x < 0 the quotient e/(1+e) rounds
-    # numerator and denominator separately, which can dip by one ulp.
+    # Non-decreasing up to one ulp: e = RN(p(w) * 2^n) is a polynomial
+    # approximation whose last bit can step back where n changes or p's
+    # error turns, and RN(1 / RN(1 + e)) can pass that step on as one ulp.
     dips = s[:-1] - s[1:]
     assert np.all(dips <= np.spacing(s[:-1]))
-    assert np.all(s[x >= 0][:-1] <= s[x >= 0][1:])  # 1/(1+e) is monotone
+    # for x >= 0 (e <= 1, absorbed by 1 + e) no dip occurs on this grid
+    assert np.all(s[x >= 0][:-1] <= s[x >= 0][1:])
     assert np.all((s >= 0) & (s <= 1))

@@ -191,7 +191,8 @@ class FullStep:
         self.launches_per_layer = {"eqb": 4, "lei": 2}
         self.hi_events = []
 
-    def layer(self, l, logits=None, grad=None, lei=True, time_hi=False, join=False):
+    def layer(self, l, logits=None, grad=None, lei=True, time_hi=False, join=False,
+              per_microbatch=False):
         """One layer.  EQB runs on the current stream.  LEI needs only this
         layer's top-k sets: its rho kernel runs on a second stream beside the
         EQB tail, and its grad update is enqueued right behind the NEXT
@@ -210,8 +211,17 @@ class FullStep:
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record()
         # the top-k sets are LEI's input only: EQB alone does not produce them
-        qb.qb_route_hist_hi(lg, self.bias[l], w.k, self.hist_hi[l], keys_out=self.keys,
-                            topk_out=self.topk[j] if lei else None)
+        if per_microbatch:
+            # one hi-pass call per 32768-token microbatch, as they would arrive
+            n = w.n_tokens
+            for m in range(w.n_micro):
+                sl = slice(m * n, (m + 1) * n)
+                qb.qb_route_hist_hi(lg[sl], self.bias[l], w.k, self.hist_hi[l],
+                                    keys_out=self.keys[sl],
+                                    topk_out=self.topk[j][sl] if lei else None)
+        else:
+            qb.qb_route_hist_hi(lg, self.bias[l], w.k, self.hist_hi[l], keys_out=self.keys,
+                                topk_out=self.topk[j] if lei else None)
         if time_hi:
             e1.record()
             self.hi_events.append((e0, e1))
@@ -244,11 +254,11 @@ class FullStep:
             self.qb.lei_apply(g, self.ws[j], batch_tokens=self.w.n_tokens)
             self.pending = None
 
-    def step(self, lei=True, time_hi=False):
+    def step(self, lei=True, time_hi=False, per_microbatch=False):
         main = torch.cuda.current_stream()
         self.side.wait_stream(main)
         for l in range(self.L):
-            self.layer(l, lei=lei, time_hi=time_hi)
+            self.layer(l, lei=lei, time_hi=time_hi, per_microbatch=per_microbatch)
         self.flush()
         main.wait_stream(self.side)
 
@@ -629,6 +639,9 @@ def main():
     ms_hi_loop = _timed(lambda: fs.step(lei=True, time_hi=True), 1, 0, dist_on)
     hi_ms = [a.elapsed_time(b) for a, b in fs.hi_events]
     ms_eqb = _timed(graphed(lambda: fs.step(lei=False)), args.steps, args.warmup, dist_on)
+    # the same EQB step with the hi pass called once per 32768-token microbatch
+    ms_eqb_mb = _timed(graphed(lambda: fs.step(lei=False, per_microbatch=True)), args.steps,
+                       args.warmup, dist_on)
     ms_step = ms / args.steps
     value = world * tokens_layer_step / (ms_step / 1e3)
     eqb_value = world * tokens_layer_step / ((ms_eqb / args.steps) / 1e3)
@@ -718,7 +731,14 @@ def main():
                        "cuda_graph": not args.no_graph,
                        "l2": f"resident logits + gradients ({2 * fs.L * n * E * 4 / 2**30:g} GiB) "
                              "larger than L2 (129 MB); no flush"},
-            "eqb_only": {"value": eqb_value, "unit": UNIT, "ms_per_step": ms_eqb / args.steps},
+            "eqb_only": {"value": eqb_value, "unit": UNIT, "ms_per_step": ms_eqb / args.steps,
+                         "hi_pass_calls_per_layer": 1,
+                         "frac": eqb_bytes * fs.L / ((ms_eqb / args.steps) / 1e3) / 1e9 / peak},
+            # the same with one hi-pass call per 32768-token microbatch (16 per layer)
+            "eqb_only_per_microbatch": {
+                "value": world * tokens_layer_step / ((ms_eqb_mb / args.steps) / 1e3), "unit": UNIT,
+                "ms_per_step": ms_eqb_mb / args.steps, "hi_pass_calls_per_layer": w.n_micro,
+                "frac": eqb_bytes * fs.L / ((ms_eqb_mb / args.steps) / 1e3) / 1e9 / peak},
             # whole-path HBM roofline: algorithmic bytes of every kernel of a layer
             # (hi pass 1560 B/token, lo pass 512, LEI counts 24, LEI apply 2048)
             # over the measured step time

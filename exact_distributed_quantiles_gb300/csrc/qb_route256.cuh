@@ -124,6 +124,33 @@ __device__ __forceinline__ void group_v(const unsigned char* row, const float* b
   f2_unpack(f2_sub(f2_pack(b1.z, b1.w), f2_pack(s1.z, s1.w)), v[6], v[7]);
 }
 
+// Half `half` of group g of a row (4 negated scores) -> v = b - sn.
+__device__ __forceinline__ void half_v(const unsigned char* row, const float* bias_s, int g,
+                                       int half, float (&v)[4]) {
+  const float4 s0 = *reinterpret_cast<const float4*>(row + 512 * half + 16 * g);
+  const float4 b0 = *reinterpret_cast<const float4*>(bias_s + 128 * half + 4 * g);
+  f2_unpack(f2_sub(f2_pack(b0.x, b0.y), f2_pack(s0.x, s0.y)), v[0], v[1]);
+  f2_unpack(f2_sub(f2_pack(b0.z, b0.w), f2_pack(s0.z, s0.w)), v[2], v[3]);
+}
+
+// Merge 4 values into the descending list L (KL >= 8): sort them (5
+// comparators), then L[i] = max(L[i], B[KL-1-i]) against the 4 sorted values
+// padded with -inf (only the last 4 positions change) and a bitonic merger.
+template <int KL>
+__device__ __forceinline__ void merge_block4(float (&L)[KL], float (&v)[4]) {
+  route::cas_desc(v[0], v[1]); route::cas_desc(v[2], v[3]);
+  route::cas_desc(v[0], v[2]); route::cas_desc(v[1], v[3]);
+  route::cas_desc(v[1], v[2]);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) L[KL - 4 + j] = fmaxf(L[KL - 4 + j], v[3 - j]);
+#pragma unroll
+  for (int d = KL / 2; d >= 1; d /= 2) {
+#pragma unroll
+    for (int i = 0; i < KL; ++i)
+      if ((i & d) == 0) route::cas_desc(L[i], L[i + d]);
+  }
+}
+
 // Expert of element i (0..7) of lane L.
 __device__ __forceinline__ int expert_of(int lane, int i) {
   return (i < 4) ? 4 * lane + i : 128 + 4 * lane + (i - 4);
@@ -157,20 +184,47 @@ struct Ctx {
   int k;
 };
 
-// Issue the loads of row pair q of the tile at token `start` (nrows rows).
+// Issue the loads of row pair q of the tile at token `start` (nrows rows):
+// every lane copies its 16-byte chunks of the pair with cp.async (global to
+// shared, no registers) and then makes the pair's mbarrier track their
+// completion (cp.async.mbarrier.arrive.noinc; the barrier expects one such
+// arrival per lane).  The copies go through the load/store path, not the
+// bulk-copy unit: that unit stays free for the bulk reductions of a kernel
+// running beside this one (lei_apply_overlap), which stalled badly behind
+// one bulk copy per row.
 template <typename T>
 __device__ __forceinline__ void issue_pair(const Ctx& c, int64_t start, int nrows, int q) {
+  constexpr int kChunks = In<T>::kRowBytes / 16;  // 16-byte chunks per row
   const int r0 = 2 * q;
-  if (nrows <= r0) return;
+  if (nrows <= r0) return;  // warp-uniform
   const int nr = nrows - r0 >= 2 ? 2 : 1;
-  if (c.lane == 0) {
-    const T* src = static_cast<const T*>(c.a->logits) + (start + r0) * (int64_t)kE;
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(c.bars + q, (uint32_t)(nr * In<T>::kRowBytes));
-    bulk_g2s(c.tile + r0 * kPitch + In<T>::kOff, src, In<T>::kRowBytes, c.bars + q);
-    if (nr == 2)
-      bulk_g2s(c.tile + (r0 + 1) * kPitch + In<T>::kOff, src + kE, In<T>::kRowBytes, c.bars + q);
+  const char* src = reinterpret_cast<const char*>(static_cast<const T*>(c.a->logits) +
+                                                  (start + r0) * (int64_t)kE);
+  const uint32_t dst = smem_u32(c.tile + r0 * kPitch + In<T>::kOff);
+#pragma unroll
+  for (int j = 0; j < 2 * kChunks / 32; ++j) {
+    const int ch = c.lane + 32 * j;  // chunk of the pair
+    const int row = ch / kChunks;
+    if (row < nr)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                       dst + (uint32_t)(row * kPitch + (ch % kChunks) * 16)),
+                   "l"(src + row * In<T>::kRowBytes + (ch % kChunks) * 16)
+                   : "memory");
   }
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(c.bars + q))
+               : "memory");
+}
+
+// Bounded wait on an mbarrier phase, decided by the whole warp at once (a
+// vote per poll keeps the loop warp-uniform); gives up after ~2^24 polls,
+// records kDevTimeout and returns false.
+__device__ __forceinline__ bool warp_wait_bounded(uint64_t* bar, uint32_t parity, int* status) {
+  for (uint32_t it = 0; it < (1u << 24); ++it) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    if (it > 64) __nanosleep(64);
+  }
+  if (lane_id() == 0) atomicOr(status, kDevTimeout);
+  return false;
 }
 
 // Phase C of a tile: r = alpha + sn (= alpha - s), BF16 keys, key stores and
@@ -220,8 +274,7 @@ __device__ __forceinline__ void phase_c(const Ctx& c, int64_t t0, int rows, int6
         }
       }
     }
-    const bool oow = mslot == (uint32_t)kDummy;
-    if (__any_sync(0xffffffffu, oow) && oow) {
+    if (__any_sync(0xffffffffu, mslot == (uint32_t)kDummy)) {
       // rare: hi bytes outside the shared window go to the global histogram
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
@@ -264,8 +317,8 @@ __device__ __forceinline__ bool tile_pass(const Ctx& c, const float (&breg)[8], 
   bool ok = true;
 #pragma unroll 1
   for (int q = 0; q < kPairs; ++q) {
-    if (FULL || 2 * q < rows) ok = mbar_wait_bounded(c.bars + q, parity, a.status);
-    if (!__all_sync(0xffffffffu, ok)) return false;
+    if (FULL || 2 * q < rows) ok = warp_wait_bounded(c.bars + q, parity, a.status);
+    if (!ok) return false;
     unsigned char* r0 = tile + 2 * q * kPitch;
     float x[16];
     load_x(r0, lane, static_cast<const T*>(nullptr), x);
@@ -355,14 +408,36 @@ __device__ __forceinline__ bool tile_pass(const Ctx& c, const float (&breg)[8], 
       for (int i = 0; i < 8; ++i) w8[i] = gr[0] < 0 ? -INFINITY : w8[i];
       route::first_block8<KL>(L, w8);
     }
+    // k = 6 (at most 6 groups): the second round deals the halves of the
+    // groups of rank 4 and 5 (lane h: rank 4 + h/2, half h%2), so that every
+    // lane sorts 4 values instead of two lanes sorting 8 each.
+    int g1 = -1, half1 = 0;
+    if constexpr (K1 == 7) {
+      uint32_t m = gt;
 #pragma unroll
-    for (int r = 1; r < R; ++r) {
-      if (__any_sync(0xffffffffu, gr[r] >= 0)) {
-        float w8[8];
-        group_v(trow, c.bias_s, gr[r] < 0 ? 0 : gr[r], w8);
+      for (int p = 0; p < 4; ++p) m &= m - 1;
+      const int g4 = route::lowest_bit(m);
+      m &= m - 1;
+      const int g5 = route::lowest_bit(m);
+      g1 = (h >> 1) ? g5 : g4;
+      half1 = h & 1;
+      if (__any_sync(0xffffffffu, g1 >= 0)) {
+        float w4[4];
+        half_v(trow, c.bias_s, g1 < 0 ? 0 : g1, half1, w4);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) w8[i] = gr[r] < 0 ? -INFINITY : w8[i];
-        route::merge_block8<KL>(L, w8);
+        for (int i = 0; i < 4; ++i) w4[i] = g1 < 0 ? -INFINITY : w4[i];
+        merge_block4<KL>(L, w4);
+      }
+    } else {
+#pragma unroll
+      for (int r = 1; r < R; ++r) {
+        if (__any_sync(0xffffffffu, gr[r] >= 0)) {
+          float w8[8];
+          group_v(trow, c.bias_s, gr[r] < 0 ? 0 : gr[r], w8);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w8[i] = gr[r] < 0 ? -INFINITY : w8[i];
+          route::merge_block8<KL>(L, w8);
+        }
       }
     }
     route::merge_partner<KL>(L, 8);
@@ -403,6 +478,50 @@ __device__ __forceinline__ bool tile_pass(const Ctx& c, const float (&breg)[8], 
             }
           }
         }
+      } else if constexpr (K1 == 7) {
+        // the 6 experts with v > alpha, ascending.  Pieces in expert order:
+        // the low halves of ranks 0-3 (round 0, lanes 0-3), of rank 4 (lane 0)
+        // and 5 (lane 2), then the high halves of ranks 0-3, 4 (lane 1), 5
+        // (lane 3).  Packed 8-bit counts per lane: A = round-0 low half,
+        // B = round-0 high half, Ce / Co = the round-1 half on even / odd lanes.
+        uint32_t b0lo = 0, b0hi = 0, b1 = 0;
+        {
+          float w8[8];
+          group_v(trow, c.bias_s, gr[0] < 0 ? 0 : gr[0], w8);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            b0lo |= (w8[i] > alpha ? 1u : 0u) << i;
+            b0hi |= (w8[4 + i] > alpha ? 1u : 0u) << i;
+          }
+          if (gr[0] < 0 || !actB) b0lo = b0hi = 0u;
+        }
+        if (__any_sync(0xffffffffu, g1 >= 0)) {
+          float w4[4];
+          half_v(trow, c.bias_s, g1 < 0 ? 0 : g1, half1, w4);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) b1 |= (w4[i] > alpha ? 1u : 0u) << i;
+          if (g1 < 0 || !actB) b1 = 0u;
+        }
+        const uint32_t c1 = (uint32_t)__popc(b1);
+        const uint32_t cnt = (uint32_t)__popc(b0lo) | ((uint32_t)__popc(b0hi) << 8) |
+                             ((half1 ? 0u : c1) << 16) | ((half1 ? c1 : 0u) << 24);
+        uint32_t incl = cnt;
+        {
+          uint32_t y = __shfl_up_sync(0xffffffffu, incl, 8);
+          if (h >= 1) incl += y;
+          y = __shfl_up_sync(0xffffffffu, incl, 16);
+          if (h >= 2) incl += y;
+        }
+        const uint32_t tot = __shfl_sync(0xffffffffu, incl, t + 24);
+        const uint32_t excl = incl - cnt;
+        const int totA = (int)(tot & 0xFFu), totB = (int)((tot >> 8) & 0xFFu);
+        const int base_hi = totA + (int)((tot >> 16) & 0xFFu);
+        int pos = (int)(excl & 0xFFu);
+        for (uint32_t b = b0lo; b; b &= b - 1) out[pos++] = 4 * gr[0] + __ffs((int)b) - 1;
+        pos = base_hi + (int)((excl >> 8) & 0xFFu);
+        for (uint32_t b = b0hi; b; b &= b - 1) out[pos++] = 128 + 4 * gr[0] + __ffs((int)b) - 1;
+        pos = half1 ? base_hi + totB + (int)(excl >> 24) : totA + (int)((excl >> 16) & 0xFFu);
+        for (uint32_t b = b1; b; b &= b - 1) out[pos++] = 128 * half1 + 4 * g1 + __ffs((int)b) - 1;
       } else {
         // the k experts with v > alpha, ascending: every lane's dealt groups
         // in dealing order (ascending group index), low halves first
@@ -500,7 +619,8 @@ __global__ void __launch_bounds__(warps_max(MODE) * 32, 1) route256_kernel(const
   asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int i = threadIdx.x; i < kE; i += blockDim.x) bias_s[i] = a.bias[i];
   if (lane == 0) {
-    for (int q = 0; q < kPairs; ++q) mbar_init(c.bars + q, 1);
+    // one arrival per lane per phase: each lane's cp.async completions
+    for (int q = 0; q < kPairs; ++q) mbar_init(c.bars + q, 32);
     fence_mbar_init();
   }
   __syncthreads();

@@ -151,6 +151,25 @@ __device__ __forceinline__ void merge_block4(float (&L)[KL], float (&v)[4]) {
   }
 }
 
+// The M-th largest (1-based) of the union of this lane's descending list L
+// and the list of lane ^ o, without merging them: for two descending lists A
+// and B it is max over i in [0, M] of min(A[i-1], B[M-1-i]), out-of-range
+// entries being +inf.  Only the partner's first M entries travel.
+template <int KL, int M>
+__device__ __forceinline__ float select_with_partner(const float (&L)[KL], const float (&P)[KL]) {
+  static_assert(M >= 1 && M <= KL, "rank out of range");
+  float best = fmaxf(P[M - 1], L[M - 1]);  // i = 0 and i = M
+#pragma unroll
+  for (int i = 1; i < M; ++i) best = fmaxf(best, fminf(L[i - 1], P[M - 1 - i]));
+  return best;
+}
+
+template <int KL, int M>
+__device__ __forceinline__ void partner_head(const float (&L)[KL], float (&P)[KL], int o) {
+#pragma unroll
+  for (int i = 0; i < KL; ++i) P[i] = i < M ? __shfl_xor_sync(0xffffffffu, L[i], o) : -INFINITY;
+}
+
 // Expert of element i (0..7) of lane L.
 __device__ __forceinline__ int expert_of(int lane, int i) {
   return (i < 4) ? 4 * lane + i : 128 + 4 * lane + (i - 4);
@@ -379,8 +398,15 @@ __device__ __forceinline__ bool tile_pass(const Ctx& c, const float (&breg)[8], 
       route::first_block8<KL>(L, w8);
     }
     route::merge_partner<KL>(L, 8);
-    route::merge_partner<KL>(L, 16);
-    const float tau = route::pick<KL, K1>(L, k);
+    float tau;
+    if constexpr (K1 > 0) {
+      float P[KL];
+      partner_head<KL, K1>(L, P, 16);
+      tau = select_with_partner<KL, K1>(L, P);
+    } else {
+      route::merge_partner<KL>(L, 16);
+      tau = route::pick<KL, K1>(L, k);
+    }
     uint32_t gt = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) gt |= (gm[i] > tau ? 1u : 0u) << (8 * h + i);
@@ -441,19 +467,31 @@ __device__ __forceinline__ bool tile_pass(const Ctx& c, const float (&breg)[8], 
       }
     }
     route::merge_partner<KL>(L, 8);
-    route::merge_partner<KL>(L, 16);
-    const float alpha = fmaxf(tau, route::pick<KL, K1>(L, k));
+    // alpha = max(tau, the (k+1)-th largest v of the dealt groups); ties at
+    // alpha exist exactly when the k-th largest of those is not above it
+    float alpha;
+    bool tie;
+    if constexpr (K1 > 0) {
+      float P[KL];
+      partner_head<KL, K1>(L, P, 16);
+      alpha = fmaxf(tau, select_with_partner<KL, K1>(L, P));
+      tie = !(select_with_partner<KL, K1 - 1>(L, P) > alpha);
+    } else {
+      route::merge_partner<KL>(L, 16);
+      alpha = fmaxf(tau, route::pick<KL, K1>(L, k));
+      int c_gt = 0;
+#pragma unroll
+      for (int i = 0; i < KL; ++i) c_gt += (i < k && L[i] > alpha) ? 1 : 0;
+      tie = c_gt < k;
+    }
     const int64_t tok = t0 + t;
     if (actB && h == 0) {
       c.alpha_s[t] = alpha;
       if (a.alpha_out) a.alpha_out[tok] = alpha;
     }
     if (MODE == kHi256 && a.topk_out) {
-      int c_gt = 0;
-#pragma unroll
-      for (int i = 0; i < KL; ++i) c_gt += (i < k && L[i] > alpha) ? 1 : 0;
       int32_t* out = a.topk_out + tok * k;
-      if (__any_sync(0xffffffffu, actB && c_gt < k)) {
+      if (__any_sync(0xffffffffu, actB && tie)) {
         // rare: ties at alpha.  One lane per token scans the groups whose
         // maximum reaches alpha in expert order (low halves, then high).
         uint32_t ge = 0;
@@ -462,7 +500,18 @@ __device__ __forceinline__ bool tile_pass(const Ctx& c, const float (&breg)[8], 
         ge |= __shfl_xor_sync(0xffffffffu, ge, 8);
         ge |= __shfl_xor_sync(0xffffffffu, ge, 16);
         if (actB && h == 0) {
-          int tl = k - c_gt, n = 0;
+          // k minus the number of v > alpha: the ties to take, in index order
+          int tl = k;
+          for (uint32_t m = ge; m; m &= m - 1) {
+            const int g = route::lowest_bit(m);
+            for (int half = 0; half < 2; ++half)
+              for (int i = 0; i < 4; ++i) {
+                const int e = half * 128 + 4 * g + i;
+                const float sv = *reinterpret_cast<const float*>(trow + 4 * e);
+                tl -= __fsub_rn(c.bias_s[e], sv) > alpha ? 1 : 0;
+              }
+          }
+          int n = 0;
           for (int half = 0; half < 2; ++half) {
             for (uint32_t m = ge; m; m &= m - 1) {
               const int g = route::lowest_bit(m);

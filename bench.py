@@ -492,9 +492,9 @@ def components(qb, inputs, dev, reps, warmup, peak_hbm, peaks):
 
 
 def cpu_baseline_sample(n_tokens: int, layer: int = 0, threads: int | None = None):
-    """Oracle on a bounded sample: n_tokens of one full-step layer through EQB
-    (route by full sort, keys, hi/lo counts, exact select by sort, centering)
-    and LEI per 32768-token local batch.  threads: OpenMP threads for the
+    """Oracle on a bounded sample: n_tokens of one full-step layer through the
+    two-pass EQB of the headline metric (route by full sort, keys, hi/lo
+    counts, exact select by sort, centering).  threads: OpenMP threads for the
     oracle (None: all cores).  Returns (seconds, tokens, threads used)."""
     import oracle
     from exact_distributed_quantiles_gb300 import inputs
@@ -503,10 +503,8 @@ def cpu_baseline_sample(n_tokens: int, layer: int = 0, threads: int | None = Non
     ws = inputs.scaled(w, n_micro=max(1, n_tokens // w.n_tokens),
                        n_tokens=min(n_tokens, w.n_tokens))
     bias, mbs = inputs.router_layer(ws, inputs.seed_for(WORKLOAD, layer))
-    grad = inputs.score_grad(ws, inputs.seed_for(WORKLOAD, layer), n_tokens=ws.n_tokens)
     mbs_np = [m.numpy() for m in mbs]
     b_np = bias.numpy()
-    g_np = grad.numpy()
     all_cores = oracle.num_threads()
     if threads is not None:
         oracle.set_num_threads(threads)
@@ -514,9 +512,6 @@ def cpu_baseline_sample(n_tokens: int, layer: int = 0, threads: int | None = Non
         used = oracle.num_threads()
         t0 = time.perf_counter()
         oracle.eqb_global_batch(mbs_np, b_np, ws.k)
-        for m in mbs_np:
-            t = oracle.route(m, b_np, ws.k, want=("topk",))["topk"]
-            oracle.lei(g_np, t, ws.eta)
         dt = time.perf_counter() - t0
     finally:
         oracle.set_num_threads(all_cores)
@@ -547,7 +542,7 @@ def run_reference(args):
                    "sample_tokens_per_step": n_tok},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{n_tok} tokens of full-step layer 0: EQB (full-sort routing, "
-                                   "keys, counts, sort select, centering) + LEI"},
+                                   "keys, counts, sort select, centering)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -571,7 +566,8 @@ def main():
                          "captured once as a CUDA graph")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=[WORKLOAD, "k3", "router_gemm", "rank_average", "maxvio"],
-                    help="full_step (the headline line) or one of the other timed paths alone")
+                    help="full_step (the headline line: EQB step, with LEI in full_step) or one "
+                         "of the other timed paths alone")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -632,18 +628,22 @@ def main():
         return graph.replay
 
     graphs = []
-    step_fn = graphed(lambda: fs.step(lei=True))
+    # the headline: the two-pass EQB step (per layer: hi pass over the layer's
+    # 16 microbatches, select, lo pass over the keys, finalize = bias update
+    # and histogram reset)
+    eqb_fn = graphed(lambda: fs.step(lei=False))
     with ClockSampler(local) as clk:
-        ms = _timed(step_fn, args.steps, args.warmup, dist_on)
+        ms_eqb = _timed(eqb_fn, args.steps, args.warmup, dist_on)
     fs.hi_events.clear()
     ms_hi_loop = _timed(lambda: fs.step(lei=True, time_hi=True), 1, 0, dist_on)
     hi_ms = [a.elapsed_time(b) for a, b in fs.hi_events]
-    ms_eqb = _timed(graphed(lambda: fs.step(lei=False)), args.steps, args.warmup, dist_on)
-    # the same EQB step with the hi pass called once per 32768-token microbatch
+    # the full step of the workload: EQB + LEI (eta=8e-5) per 32768-token batch
+    ms = _timed(graphed(lambda: fs.step(lei=True)), args.steps, args.warmup, dist_on)
+    # the EQB step with the hi pass called once per 32768-token microbatch
     ms_eqb_mb = _timed(graphed(lambda: fs.step(lei=False, per_microbatch=True)), args.steps,
                        args.warmup, dist_on)
     ms_step = ms / args.steps
-    value = world * tokens_layer_step / (ms_step / 1e3)
+    full_value = world * tokens_layer_step / (ms_step / 1e3)
     eqb_value = world * tokens_layer_step / ((ms_eqb / args.steps) / 1e3)
 
     peak, peak_kind, peaks = _peaks()
@@ -654,51 +654,43 @@ def main():
     step_bytes = hi_bytes + n * E * 2 + n * k * 4 + n * E * 4 * 2  # + LEI counts, grad R/W
     achieved = hi_bytes / (hi_avg_ms / 1e3) / 1e9
 
-    # end to end through host buffers: per layer H2D logits + grad, D2H grad + bias
+    # end to end through host buffers: the EQB step with every layer's logits
+    # copied in from pinned host memory and its new bias copied out
     e2e = None
     if not args.no_e2e:
         lg_h = fs.logits[0].cpu().pin_memory()
-        gr_h = fs.grads[0].cpu().pin_memory()
-        gr_out = torch.empty_like(gr_h).pin_memory()
         b_out = torch.empty(fs.L, E, dtype=torch.float32).pin_memory()
-        # two device buffer sets; layer l+1's inputs are copied in on one
-        # stream and layer l-1's gradient and bias copied out on another
-        # while layer l computes
+        # two device buffers; layer l+1's logits are copied in on one stream
+        # and layer l's bias out on another while layer l computes
         d_lg = [torch.empty_like(fs.logits[0]) for _ in range(2)]
-        d_gr = [torch.empty_like(fs.grads[0]) for _ in range(2)]
         s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
         comp = torch.cuda.current_stream()
         ev_in = [torch.cuda.Event() for _ in range(2)]
         ev_done = [torch.cuda.Event() for _ in range(2)]
-        ev_free = [torch.cuda.Event() for _ in range(2)]
 
         def e2e_step():
             s_in.wait_stream(comp)
             s_out.wait_stream(comp)
-            fs.side.wait_stream(comp)
             for l in range(fs.L):
                 j = l & 1
                 with torch.cuda.stream(s_in):
                     if l >= 2:
-                        s_in.wait_event(ev_free[j])
+                        s_in.wait_event(ev_done[j])  # layer l-2 has read this buffer
                     d_lg[j].copy_(lg_h, non_blocking=True)
-                    d_gr[j].copy_(gr_h, non_blocking=True)
                     ev_in[j].record(s_in)
                 comp.wait_event(ev_in[j])
-                fs.layer(l, logits=d_lg[j], grad=d_gr[j], join=True)
+                fs.layer(l, logits=d_lg[j], lei=False)
                 ev_done[j].record(comp)
                 with torch.cuda.stream(s_out):
                     s_out.wait_event(ev_done[j])
-                    gr_out.copy_(d_gr[j], non_blocking=True)
                     b_out[l].copy_(fs.bias[l], non_blocking=True)
-                    ev_free[j].record(s_out)
             comp.wait_stream(s_out)  # the step ends with its last copy out
 
         e2e_steps = max(1, min(args.steps, 3))
         ms_e2e = _timed(e2e_step, e2e_steps, 1, dist_on)
         e2e = {"value": world * tokens_layer_step / ((ms_e2e / e2e_steps) / 1e3), "unit": UNIT,
-               "h2d_bytes_per_step": fs.L * 2 * n * E * 4,
-               "d2h_bytes_per_step": fs.L * (n * E * 4 + E * 4), "steps": e2e_steps}
+               "h2d_bytes_per_step": fs.L * n * E * 4, "d2h_bytes_per_step": fs.L * E * 4,
+               "steps": e2e_steps}
 
     comps = None
     if not args.no_components:
@@ -711,37 +703,48 @@ def main():
         dt1, nt1, _ = cpu_baseline_sample(args.cpu_tokens_single, threads=1)
         cpu = {"value": nt / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"{nt} tokens of full-step layer 0 through the oracle's EQB "
-                         "(full-sort routing, keys, counts, sort select, centering) + LEI "
+                         "(full-sort routing, keys, counts, sort select, centering) "
                          f"({dt:.1f} s on {cores} threads)",
                "single_thread": {"value": nt1 / dt1, "unit": UNIT, "cores": 1,
                                  "sample": f"{nt1} tokens of the same layer, one thread "
                                            f"({dt1:.1f} s)"}}
 
     if rank == 0:
+        eqb_ms_step = ms_eqb / args.steps
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "metric": METRIC, "value": eqb_value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": eqb_ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
             "config": {"workload": f"{WORKLOAD}: {fs.L} layers x {w.n_micro}x{w.n_tokens} tokens, "
-                                   f"E={E}, k={k}; per layer EQB hi pass + select + lo pass + "
-                                   "finalize (bias update, reset) + LEI (eta=8e-5) per 32768-token "
-                                   "local batch",
+                                   f"E={E}, k={k}; a step = per layer the two-pass EQB: hi pass "
+                                   "over the layer's 16 microbatches (one call), select, lo pass "
+                                   "over the stored keys, finalize (bias update, histogram reset); "
+                                   "LEI timed in full_step",
                        "layers": fs.L, "tokens_per_layer": n, "E": E, "k": k,
                        "parallelism": f"replicas x{world} (token shards, no collective)",
                        "cuda_graph": not args.no_graph,
-                       "l2": f"resident logits + gradients ({2 * fs.L * n * E * 4 / 2**30:g} GiB) "
-                             "larger than L2 (129 MB); no flush"},
-            "eqb_only": {"value": eqb_value, "unit": UNIT, "ms_per_step": ms_eqb / args.steps,
-                         "hi_pass_calls_per_layer": 1,
-                         "frac": eqb_bytes * fs.L / ((ms_eqb / args.steps) / 1e3) / 1e9 / peak},
-            # the same with one hi-pass call per 32768-token microbatch (16 per layer)
-            "eqb_only_per_microbatch": {
+                       "l2": f"resident logits ({fs.L * n * E * 4 / 2**30:g} GiB) larger than L2 "
+                             "(129 MB); no flush"},
+            # HBM roofline of the EQB step: 2048 algorithmic bytes per token
+            # (logits read, keys written and read back)
+            "eqb_roofline": {"bytes_per_layer": eqb_bytes,
+                             "achieved": eqb_bytes * fs.L / (eqb_ms_step / 1e3) / 1e9,
+                             "peak": peak, "unit": "GB/s",
+                             "frac": eqb_bytes * fs.L / (eqb_ms_step / 1e3) / 1e9 / peak,
+                             "frac_nominal": eqb_bytes * fs.L / (eqb_ms_step / 1e3) / 1e9
+                             / NOMINAL_HBM_GBS},
+            # the same EQB step with one hi-pass call per 32768-token microbatch
+            "eqb_per_microbatch": {
                 "value": world * tokens_layer_step / ((ms_eqb_mb / args.steps) / 1e3), "unit": UNIT,
                 "ms_per_step": ms_eqb_mb / args.steps, "hi_pass_calls_per_layer": w.n_micro,
                 "frac": eqb_bytes * fs.L / ((ms_eqb_mb / args.steps) / 1e3) / 1e9 / peak},
-            # whole-path HBM roofline: algorithmic bytes of every kernel of a layer
-            # (hi pass 1560 B/token, lo pass 512, LEI counts 24, LEI apply 2048)
-            # over the measured step time
+            # the full step of the workload: EQB + LEI (eta = 8e-5) per 32768-token
+            # local batch (rho beside the EQB tail, grad update beside the next
+            # layer's hi pass)
+            "full_step": {"value": full_value, "unit": UNIT, "ms_per_step": ms_step,
+                          "gpu_launches_per_step": fs.L * (fs.launches_per_layer["eqb"]
+                                                           + fs.launches_per_layer["lei"])},
             "step_roofline": {
                 "bytes_per_layer": step_bytes, "eqb_bytes_per_layer": eqb_bytes,
                 "achieved": step_bytes * fs.L / (ms_step / 1e3) / 1e9,
@@ -767,8 +770,7 @@ def main():
             "cpu_baseline": cpu,
             "e2e": e2e,
             "components": comps,
-            "gpu_launches": args.steps * fs.L * (fs.launches_per_layer["eqb"]
-                                                 + fs.launches_per_layer["lei"]),
+            "gpu_launches": args.steps * fs.L * fs.launches_per_layer["eqb"],
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)

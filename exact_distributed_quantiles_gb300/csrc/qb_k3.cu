@@ -77,9 +77,9 @@ __device__ __forceinline__ void load8x(const __nv_bfloat16* p, float (&x)[8]) {
 template <typename T, bool GLOBAL>
 __global__ void __launch_bounds__(kCountThreads, 1)
     k3_count_kernel(const T* __restrict__ logits, const float* __restrict__ alpha, int64_t N,
-                    int E, const float* __restrict__ bounds, int nbins, int pitch,
+                    int E, const float* __restrict__ bounds, int nbins, int pitch, int bulk,
                     int32_t* __restrict__ hist, int64_t rows_per_cta) {
-  extern __shared__ int32_t h[];
+  extern __shared__ __align__(16) int32_t h[];
   constexpr int kWarps = kCountThreads / 32;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -102,40 +102,39 @@ __global__ void __launch_bounds__(kCountThreads, 1)
 
   const f2_t LO = f2_splat(lo), SC = f2_splat(scale);
   const T* base = logits + e0;
-  int64_t r = r_begin + warp * 8 + rsub;
   const int64_t stride = (int64_t)kWarps * 8;
-  float x[8], a = 0.0f;
-  bool act = r < r_end;
-  if (act) {
-    load8x(base + r * E, x);
-    a = __ldg(alpha + r);
-  }
-  while (__any_sync(0xffffffffu, act)) {
-    // next rows in flight while this one is counted
-    const int64_t rn = r + stride;
-    const bool actn = rn < r_end;
-    float xn[8], an = 0.0f;
-    if (actn) {
-      load8x(base + rn * E, xn);
-      an = __ldg(alpha + rn);
-    }
-    if (!act) {
+  // three rows per lane in flight: the one being counted and the next two
+  constexpr int kD = 3;
+  float x[kD][8], a[kD];
+  bool act[kD];
+  int64_t r = r_begin + warp * 8 + rsub;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) x[i] = 0.0f;
+  for (int d = 0; d < kD; ++d) {
+    const int64_t rd = r + d * stride;
+    act[d] = rd < r_end;
+    a[d] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[d][i] = 0.0f;
+    if (act[d]) {
+      load8x(base + rd * E, x[d]);
+      a[d] = __ldg(alpha + rd);
     }
+  }
+  while (__any_sync(0xffffffffu, act[0])) {
     float m = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[i]));
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[0][i]));
     float sn[8];
     if (__all_sync(0xffffffffu, m <= kFastAbsX)) {
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        f2_unpack(neg_sigmoid2_fast(f2_pack(x[2 * i], x[2 * i + 1])), sn[2 * i], sn[2 * i + 1]);
+        f2_unpack(neg_sigmoid2_fast(f2_pack(x[0][2 * i], x[0][2 * i + 1])), sn[2 * i],
+                  sn[2 * i + 1]);
     } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) sn[i] = -sigmoid_pinned(x[i]);
+      for (int i = 0; i < 8; ++i) sn[i] = -sigmoid_pinned(x[0][i]);
     }
-    const f2_t A = f2_splat(a);
+    const f2_t A = f2_splat(a[0]);
     int idx[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -146,7 +145,7 @@ __global__ void __launch_bounds__(kCountThreads, 1)
       idx[2 * i] = min(max(__float2int_rz(t0), 0), last);
       idx[2 * i + 1] = min(max(__float2int_rz(t1), 0), last);
     }
-    if (act) {
+    if (act[0]) {
       if constexpr (GLOBAL) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) atomicAdd(hist + (int64_t)(e0 + i) * nbins + idx[i], 1);
@@ -155,18 +154,50 @@ __global__ void __launch_bounds__(kCountThreads, 1)
         for (int i = 0; i < 8; ++i) red_shared_inc(hb + 4u * (uint32_t)(i * pitch + idx[i]));
       }
     }
-    r = rn;
-    act = actn;
-    a = an;
+    // shift the stages and load the row kD strides ahead
 #pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] = xn[i];
+    for (int d = 0; d + 1 < kD; ++d) {
+      act[d] = act[d + 1];
+      a[d] = a[d + 1];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x[d][i] = x[d + 1][i];
+    }
+    r += stride;
+    const int64_t rl = r + (kD - 1) * stride;
+    act[kD - 1] = rl < r_end;
+    a[kD - 1] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[kD - 1][i] = 0.0f;
+    if (act[kD - 1]) {
+      load8x(base + rl * E, x[kD - 1]);
+      a[kD - 1] = __ldg(alpha + rl);
+    }
   }
   if constexpr (!GLOBAL) {
-    __syncthreads();
-    for (int i = threadIdx.x; i < kEW * nbins; i += kCountThreads) {
-      const int el = i / nbins, b = i - el * nbins;
-      const int c = h[el * pitch + b];
-      if (c) atomicAdd(hist + (int64_t)(eg * kEW + el) * nbins + b, c);
+    if (bulk) {
+      // rows 16-byte aligned in shared memory and in the histogram: one bulk
+      // reduction per expert row, added in L2 (warp w: row w)
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncthreads();
+      if (lane == 0) {
+        for (int el = warp; el < kEW; el += kWarps) {
+          asm volatile(
+              "cp.reduce.async.bulk.global.shared::cta.bulk_group.add.u32 [%0], [%1], %2;" ::"l"(
+                  hist + (int64_t)(eg * kEW + el) * nbins),
+              "r"((uint32_t)__cvta_generic_to_shared(h + el * pitch)), "r"((uint32_t)(nbins * 4))
+              : "memory");
+        }
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+      }
+    } else {
+      __syncthreads();
+      for (int el = warp; el < kEW; el += kWarps) {
+        for (int b = lane; b < nbins; b += 32) {
+          const int c = h[el * pitch + b];
+          if (c) atomicAdd(hist + (int64_t)(eg * kEW + el) * nbins + b, c);
+        }
+      }
     }
   }
 }
@@ -174,7 +205,11 @@ __global__ void __launch_bounds__(kCountThreads, 1)
 template <typename T, bool GLOBAL>
 int launch_count_t(const T* logits, const float* alpha, int64_t N, int E, const float* bounds,
                    int nbins, int32_t* hist, cudaStream_t stream) {
-  const int pitch = nbins | 1;
+  // Rows of 16-byte multiples (and an odd multiple of 4 words, so that equal
+  // bins of different experts spread over the banks) when every histogram row
+  // starts on a 16-byte boundary: they are then flushed by bulk reductions.
+  const bool bulk = (nbins % 4 == 0) && (reinterpret_cast<uintptr_t>(hist) % 16 == 0);
+  const int pitch = bulk ? ((nbins + 3) & ~3) + ((((nbins + 3) / 4) % 2 == 0) ? 4 : 0) : (nbins | 1);
   const int smem = GLOBAL ? 0 : kEW * pitch * 4;
   static int attr_bytes = 0;  // per instantiation; benign race (idempotent)
   if (smem > attr_bytes) {
@@ -190,7 +225,7 @@ int launch_count_t(const T* logits, const float* alpha, int64_t N, int E, const 
   if (n_tr < 1) n_tr = 1;
   const int64_t rows_per_cta = (N + n_tr - 1) / n_tr;
   k3_count_kernel<T, GLOBAL><<<(unsigned)(n_tr * n_eg), kCountThreads, smem, stream>>>(
-      logits, alpha, N, E, bounds, nbins, pitch, hist, rows_per_cta);
+      logits, alpha, N, E, bounds, nbins, pitch, bulk ? 1 : 0, hist, rows_per_cta);
   return launch_status();
 }
 
@@ -352,7 +387,7 @@ __global__ void __cluster_dims__(kFinCluster, 1, 1) __launch_bounds__(kFinThread
 
 int launch_k3_count(const void* logits, int dtype, const float* alpha, int64_t N, int E,
                     const float* bounds, int nbins, int32_t* hist, cudaStream_t stream) {
-  const bool fits = kEW * (nbins | 1) * 4 <= kCountSmemMax;
+  const bool fits = kEW * (((nbins + 3) & ~3) + 4) * 4 <= kCountSmemMax;
   if (dtype == QB_F32) {
     const float* x = static_cast<const float*>(logits);
     return fits ? launch_count_t<float, false>(x, alpha, N, E, bounds, nbins, hist, stream)

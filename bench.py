@@ -38,23 +38,24 @@ import torch  # noqa: E402
 
 METRIC = "QB routed tokens/s per layer (E=256,k=6, 2-pass EQB) on 1 GB300; % of HBM roofline"
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one route-kernel
-# launch on a 524288-token layer, from an ncu capture of that launch.  Reported
-# only while the kernel's sources hash to the value they had when the counters
-# were taken.
-ROUTE_TRAFFIC = {"sha1": "3e4d4f59d2ed626bde6df758fd648c9a4b198f25", "tokens": 524288,
-                 "bytes": (537.009408 + 245.643264) * 1e6}
-ROUTE_SOURCES = ("qb_route.cuh", "qb_device.cuh", "qb_route_hi.cu")
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one hi-pass
+# launch (route256_kernel, keys written, no top-k output) on a 524288-token
+# layer, from an ncu capture of that launch.  Reported only while the
+# kernel's sources hash to the value they had when the counters were taken.
+ROUTE_TRAFFIC = {"sha1": "3d3dbadb2137be31abc18c958dd35f8c5bf690e4", "tokens": 524288,
+                 "bytes": (537.133312 + 233.692416) * 1e6}
+ROUTE_SOURCES = ("qb_route256.cuh", "qb_route256_f32.cu", "qb_route.cuh", "qb_device.cuh")
 # Warp instructions of the same capture (smsp__inst_executed.sum), for the
 # issue-rate roofline of this issue-bound kernel; same hash guard.
-ROUTE_INSTR = {"tokens": 524288, "warp_instructions": 177414280}
+ROUTE_INSTR = {"tokens": 524288, "warp_instructions": 127333934}
 # Warp instructions (smsp__inst_executed.sum) of one K3 microbatch of 65536
-# bf16 tokens: the routing kernel in K3 mode plus the count kernel, from an
-# ncu capture of those launches; reported while the K3 sources hash to the
-# value they had when it was taken.
-K3_INSTR = {"sha1": "a4ce8f5b660869349346fef6e33c411374a75b14", "tokens": 65536,
-            "warp_instructions": 24588544 + 7044848}
-K3_SOURCES = ("qb_route.cuh", "qb_device.cuh", "qb_route_k3.cu", "qb_k3.cu")
+# bf16 tokens: the alpha pass (route256_kernel, K3 mode) plus the count
+# kernel, from an ncu capture of those launches; reported while the K3
+# sources hash to the value they had when it was taken.
+K3_INSTR = {"sha1": "dbfb2e7cf2d880e46db7fc4cceecdae5d5abc94c", "tokens": 65536,
+            "warp_instructions": 13063568 + 16375488}
+K3_SOURCES = ("qb_route256.cuh", "qb_route256_bf16.cu", "qb_route.cuh", "qb_device.cuh",
+              "qb_k3.cu")
 UNIT = "tokens/s/layer"
 WORKLOAD = "full_step"
 NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal
@@ -333,14 +334,14 @@ def k3_component(qb, inputs, dev, reps, warmup, peak_hbm):
         "workload": "k3: 4x65536 bf16 tokens, E=256, k=8, 1000 bins",
         "value": w3.n_pool / (ms_batch / 1e3), "unit": "tokens/s", "ms_per_batch": ms_batch,
         "launches_per_batch": 2 * w3.n_micro + 1,
-        "roofline": {"bound": "hbm", "kernel": "k3_route_hist (route_kernel K3 mode + k3_count)",
+        "roofline": {"bound": "hbm", "kernel": "k3_route_hist (route256_kernel alpha pass + k3_count_kernel)",
                      "achieved": k3_bytes / (ms_hist / 1e3) / 1e9, "peak": peak_hbm,
                      "unit": "GB/s", "frac": k3_bytes / (ms_hist / 1e3) / 1e9 / peak_hbm,
                      "bytes_per_batch": k3_bytes, "hist_ms_per_batch": ms_hist},
         # both K3 passes are bound by instruction issue, not by HBM
         "roofline_issue": (None if K3_INSTR["warp_instructions"] is None
                            or _sources_sha1(K3_SOURCES) != K3_INSTR["sha1"] else {
-            "bound": "alu", "kernel": "k3_route_hist (route_kernel K3 mode + k3_count)",
+            "bound": "alu", "kernel": "k3_route_hist (route256_kernel alpha pass + k3_count_kernel)",
             "achieved": K3_INSTR["warp_instructions"] * w3.n_pool / K3_INSTR["tokens"]
             / (ms_hist / 1e3), "peak": _issue_peak(), "unit": "warp instructions/s",
             "frac": K3_INSTR["warp_instructions"] * w3.n_pool / K3_INSTR["tokens"]
@@ -380,8 +381,12 @@ def gemm_component(qb, inputs, dev, reps, warmup, peak_hbm, peaks):
 
     ms5 = _per_call_ms(gemm_batch, reps, warmup)
     ms_g = _per_call_ms(gemm_only, reps, warmup)
-    ms_f = _per_call_ms(lambda: qb.qb_router_gemm_hist_hi(hs[0], w_t, b5, w5.k, None, hi5,
-                                                          keys_out=keys5[:n]), reps, warmup)
+    def fused_only():
+        for i, h in enumerate(hs):
+            qb.qb_router_gemm_hist_hi(h, w_t, b5, w5.k, None, hi5, keys_out=keys5[i * n:(i + 1) * n])
+
+    # per microbatch, the 4 microbatches in turn (none of them in L2)
+    ms_f = _per_call_ms(fused_only, reps, warmup) / len(hs)
     qb.qb_zero_i32(hi5)
     flops = 2.0 * w5.n_pool * H * E
     gbytes = w5.n_pool * H * 2 + H * E * 2 * w5.n_micro + w5.n_pool * E * 4
@@ -634,8 +639,9 @@ def main():
     eqb_fn = graphed(lambda: fs.step(lei=False))
     with ClockSampler(local) as clk:
         ms_eqb = _timed(eqb_fn, args.steps, args.warmup, dist_on)
+    # the hi-pass launches of the same EQB step, one event pair around each
     fs.hi_events.clear()
-    ms_hi_loop = _timed(lambda: fs.step(lei=True, time_hi=True), 1, 0, dist_on)
+    ms_hi_loop = _timed(lambda: fs.step(lei=False, time_hi=True), 1, 0, dist_on)
     hi_ms = [a.elapsed_time(b) for a, b in fs.hi_events]
     # the full step of the workload: EQB + LEI (eta=8e-5) per 32768-token batch
     ms = _timed(graphed(lambda: fs.step(lei=True)), args.steps, args.warmup, dist_on)
@@ -648,10 +654,11 @@ def main():
 
     peak, peak_kind, peaks = _peaks()
     n, E, k = w.n_pool, w.E, w.k
-    hi_bytes = n * E * (4 + 2) + n * k * 4   # logits read, keys write, top-k write
+    hi_bytes = n * E * (4 + 2)               # logits read, keys write (EQB needs no top-k)
     hi_avg_ms = statistics.mean(hi_ms) if hi_ms else float("nan")
-    eqb_bytes = n * E * (4 + 2) + n * E * 2               # hi pass without top-k + lo pass
-    step_bytes = hi_bytes + n * E * 2 + n * k * 4 + n * E * 4 * 2  # + LEI counts, grad R/W
+    eqb_bytes = hi_bytes + n * E * 2                      # hi pass + lo pass over the keys
+    # + top-k write (LEI's input), LEI counts read, grad read and write
+    step_bytes = eqb_bytes + n * k * 4 + n * k * 4 + n * E * 4 * 2
     achieved = hi_bytes / (hi_avg_ms / 1e3) / 1e9
 
     # end to end through host buffers: the EQB step with every layer's logits
@@ -756,13 +763,13 @@ def main():
                 "frac_nominal": step_bytes * fs.L / (ms_step / 1e3) / 1e9 / NOMINAL_HBM_GBS,
                 "eqb_frac_nominal": eqb_bytes * fs.L / ((ms_eqb / args.steps) / 1e3) / 1e9
                 / NOMINAL_HBM_GBS},
-            "roofline": {"bound": "hbm", "kernel": "qb_route_hist_hi (route_kernel hi mode)",
+            "roofline": {"bound": "hbm", "kernel": "qb_route_hist_hi (route256_kernel, keys out, no top-k out)",
                          "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                          "unit": "GB/s", "frac": achieved / peak, "traffic": _route_traffic(n),
                          "bytes_per_launch": hi_bytes, "avg_launch_ms": hi_avg_ms},
             "roofline_issue": (None if ROUTE_INSTR["warp_instructions"] is None
                                or not _route_sources_match() else {
-                "bound": "alu", "kernel": "qb_route_hist_hi (route_kernel hi mode)",
+                "bound": "alu", "kernel": "qb_route_hist_hi (route256_kernel, keys out, no top-k out)",
                 "achieved": ROUTE_INSTR["warp_instructions"] * n / ROUTE_INSTR["tokens"]
                 / (hi_avg_ms / 1e3), "peak": _issue_peak(), "unit": "warp instructions/s",
                 "frac": ROUTE_INSTR["warp_instructions"] * n / ROUTE_INSTR["tokens"]

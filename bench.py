@@ -302,6 +302,35 @@ def _per_call_ms(fn, reps, warmup):
     return e0.elapsed_time(e1) / reps
 
 
+def _graph(fn):
+    """fn captured once as a CUDA graph (after one eager call, which sets the
+    kernels' attributes); returns its replay."""
+    fn()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cs):
+        with torch.cuda.graph(graph, stream=cs):
+            fn()
+    torch.cuda.current_stream().wait_stream(cs)
+    _graph.keep.append(graph)
+    return graph.replay
+
+
+_graph.keep = []
+
+
+def _rotating(replays):
+    """One call = the next of the given replays, in turn."""
+    it = [0]
+
+    def f():
+        replays[it[0] % len(replays)]()
+        it[0] += 1
+    return f
+
+
 def k3_component(qb, inputs, dev, reps, warmup, peak_hbm):
     """K3 histogram mode: E=256, k=8, 4 x 65536 bf16 tokens, 1000 bins; one
     global batch = four k3_route_hist calls + k3_finalize.  Four copies of the
@@ -315,25 +344,27 @@ def k3_component(qb, inputs, dev, reps, warmup, peak_hbm):
     alpha3 = torch.empty(w3.n_tokens, dtype=torch.float32, device=dev)
     b3 = bias3.clone()
     R3 = qb.rank(w3.n_pool, w3.E, w3.k)
-    it = [0]
 
-    def k3_hist_only():
-        for m in copies[it[0] % 4]:
+    def k3_hist_only(c):
+        for m in copies[c]:
             qb.k3_route_hist(m, b3, w3.k, bounds, hist3, alpha3)
-        it[0] += 1
 
-    def k3_batch():
-        k3_hist_only()
+    def k3_batch(c):
+        k3_hist_only(c)
         qb.k3_finalize(hist3, R3, bounds, b3, reset=True)
 
-    ms_batch = _per_call_ms(k3_batch, reps, warmup)
-    ms_hist = _per_call_ms(k3_hist_only, reps, warmup)
+    # each call shape captured as CUDA graphs (one per copy of the batch), so
+    # that the times are the device's, not the host's launch rate
+    ms_batch = _per_call_ms(_rotating([_graph(lambda c=c: k3_batch(c)) for c in range(4)]),
+                            reps, warmup)
+    ms_hist = _per_call_ms(_rotating([_graph(lambda c=c: k3_hist_only(c)) for c in range(4)]),
+                           reps, warmup)
     qb.qb_zero_i32(hist3)
     k3_bytes = w3.n_pool * w3.E * 2  # bf16 logits read once (algorithmic)
     return {
         "workload": "k3: 4x65536 bf16 tokens, E=256, k=8, 1000 bins",
         "value": w3.n_pool / (ms_batch / 1e3), "unit": "tokens/s", "ms_per_batch": ms_batch,
-        "launches_per_batch": 2 * w3.n_micro + 1,
+        "launches_per_batch": 2 * w3.n_micro + 1, "cuda_graph": True,
         "roofline": {"bound": "hbm", "kernel": "k3_route_hist (route256_kernel alpha pass + k3_count_kernel)",
                      "achieved": k3_bytes / (ms_hist / 1e3) / 1e9, "peak": peak_hbm,
                      "unit": "GB/s", "frac": k3_bytes / (ms_hist / 1e3) / 1e9 / peak_hbm,
@@ -379,14 +410,16 @@ def gemm_component(qb, inputs, dev, reps, warmup, peak_hbm, peaks):
         qb.qb_keys_hist_lo(keys5, sel5, lo5)
         qb.qb_finalize(hi5, lo5, sel5, rlo5, b5, reset=True)
 
-    ms5 = _per_call_ms(gemm_batch, reps, warmup)
-    ms_g = _per_call_ms(gemm_only, reps, warmup)
     def fused_only():
         for i, h in enumerate(hs):
-            qb.qb_router_gemm_hist_hi(h, w_t, b5, w5.k, None, hi5, keys_out=keys5[i * n:(i + 1) * n])
+            qb.qb_router_gemm_hist_hi(h, w_t, b5, w5.k, None, hi5,
+                                      keys_out=keys5[i * n:(i + 1) * n])
 
+    # CUDA graphs of each call shape (device times, not the host's launch rate)
+    ms5 = _per_call_ms(_graph(gemm_batch), reps, warmup)
+    ms_g = _per_call_ms(_graph(gemm_only), reps, warmup)
     # per microbatch, the 4 microbatches in turn (none of them in L2)
-    ms_f = _per_call_ms(fused_only, reps, warmup) / len(hs)
+    ms_f = _per_call_ms(_graph(fused_only), reps, warmup) / len(hs)
     qb.qb_zero_i32(hi5)
     flops = 2.0 * w5.n_pool * H * E
     gbytes = w5.n_pool * H * 2 + H * E * 2 * w5.n_micro + w5.n_pool * E * 4

@@ -111,6 +111,12 @@ __device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+// round toward zero (used to truncate by adding 2^23)
+__device__ __forceinline__ f2_t f2_add_rz(f2_t a, f2_t b) {
+  f2_t d;
+  asm("add.rz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 __device__ __forceinline__ f2_t f2_splat(float v) { return f2_pack(v, v); }
 
 // Hardware reciprocal estimate.  The .ftz form is the bare estimate; the

@@ -101,77 +101,81 @@ __global__ void __launch_bounds__(kCountThreads, 1)
   __syncthreads();
 
   const f2_t LO = f2_splat(lo), SC = f2_splat(scale);
+  // Bins from t = RN(RN(r - lo) * scale) without a float-to-int conversion:
+  // u = RZ(t + 2^23) is 2^23 + trunc(t) for 0 <= t < 2^23 (the sum is below
+  // 2^24, where float spacing is 1, and rounding toward zero truncates), and
+  // below 2^23 for t < 0; clamped to [2^23, 2^23 + nbins - 1] by fmax/fmin
+  // (which return the number for a NaN t, i.e. bin 0, as a truncating
+  // conversion would) its bit pattern is 0x4B000000 + the bin.
+  const f2_t M23 = f2_splat(8388608.0f);
+  const float u_last = 8388608.0f + (float)last;  // exact: nbins < 2^23
   const T* base = logits + e0;
   const int64_t stride = (int64_t)kWarps * 8;
-  // three rows per lane in flight: the one being counted and the next two
-  constexpr int kD = 3;
-  float x[kD][8], a[kD];
-  bool act[kD];
-  int64_t r = r_begin + warp * 8 + rsub;
+  // counter address of bin pattern u for element i: hb + 4 (i pitch) + 4 (u - 0x4B000000)
+  const uint32_t hb0 = hb - 4u * 0x4B000000u;
+  // Three row buffers used in turn (the compiler keeps them in registers
+  // without copies): row rc is counted from one while the next two rows'
+  // loads are in flight, and the freed buffer loads the row three strides on.
+  float x0[8], x1[8], x2[8];
+  float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f;
 #pragma unroll
-  for (int d = 0; d < kD; ++d) {
-    const int64_t rd = r + d * stride;
-    act[d] = rd < r_end;
-    a[d] = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) x[d][i] = 0.0f;
-    if (act[d]) {
-      load8x(base + rd * E, x[d]);
-      a[d] = __ldg(alpha + rd);
+  for (int i = 0; i < 8; ++i) x0[i] = x1[i] = x2[i] = 0.0f;
+  const int64_t w0 = r_begin + warp * 8;   // this warp's first row
+  const int64_t n_it = w0 < r_end ? (r_end - w0 + stride - 1) / stride : 0;
+  int64_t rc = w0 + rsub;                  // row counted next (this lane)
+  int64_t rl = rc;                         // row loaded next (this lane)
+  auto load = [&](float (&x)[8], float& a) {
+    if (rl < r_end) {
+      load8x(base + rl * E, x);
+      a = __ldg(alpha + rl);
     }
-  }
-  while (__any_sync(0xffffffffu, act[0])) {
+    rl += stride;
+  };
+  auto count = [&](const float (&x)[8], float a) {
     float m = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[0][i]));
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[i]));
     float sn[8];
     if (__all_sync(0xffffffffu, m <= kFastAbsX)) {
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        f2_unpack(neg_sigmoid2_fast(f2_pack(x[0][2 * i], x[0][2 * i + 1])), sn[2 * i],
-                  sn[2 * i + 1]);
+        f2_unpack(neg_sigmoid2_fast(f2_pack(x[2 * i], x[2 * i + 1])), sn[2 * i], sn[2 * i + 1]);
     } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) sn[i] = -sigmoid_pinned(x[0][i]);
+      for (int i = 0; i < 8; ++i) sn[i] = -sigmoid_pinned(x[i]);
     }
-    const f2_t A = f2_splat(a[0]);
-    int idx[8];
+    const f2_t A = f2_splat(a);
+    float u[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       // t = RN(RN(r - lo) * scale) with r = RN(alpha + sn)
       const f2_t R = f2_add(A, f2_pack(sn[2 * i], sn[2 * i + 1]));
-      float t0, t1;
-      f2_unpack(f2_mul(f2_sub(R, LO), SC), t0, t1);
-      idx[2 * i] = min(max(__float2int_rz(t0), 0), last);
-      idx[2 * i + 1] = min(max(__float2int_rz(t1), 0), last);
+      f2_unpack(f2_add_rz(f2_mul(f2_sub(R, LO), SC), M23), u[2 * i], u[2 * i + 1]);
     }
-    if (act[0]) {
-      if constexpr (GLOBAL) {
+    if (rc < r_end) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) atomicAdd(hist + (int64_t)(e0 + i) * nbins + idx[i], 1);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) red_shared_inc(hb + 4u * (uint32_t)(i * pitch + idx[i]));
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t ub = __float_as_uint(fminf(fmaxf(u[i], 8388608.0f), u_last));
+        if constexpr (GLOBAL)
+          atomicAdd(hist + (int64_t)(e0 + i) * nbins + (int)(ub - 0x4B000000u), 1);
+        else
+          red_shared_inc(hb0 + 4u * (uint32_t)(i * pitch) + 4u * ub);
       }
     }
-    // shift the stages and load the row kD strides ahead
-#pragma unroll
-    for (int d = 0; d + 1 < kD; ++d) {
-      act[d] = act[d + 1];
-      a[d] = a[d + 1];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) x[d][i] = x[d + 1][i];
-    }
-    r += stride;
-    const int64_t rl = r + (kD - 1) * stride;
-    act[kD - 1] = rl < r_end;
-    a[kD - 1] = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) x[kD - 1][i] = 0.0f;
-    if (act[kD - 1]) {
-      load8x(base + rl * E, x[kD - 1]);
-      a[kD - 1] = __ldg(alpha + rl);
-    }
+    rc += stride;
+  };
+  load(x0, a0);
+  load(x1, a1);
+  load(x2, a2);
+  for (int64_t it = 0; it < n_it; it += 3) {
+    count(x0, a0);
+    load(x0, a0);
+    if (it + 1 >= n_it) break;
+    count(x1, a1);
+    load(x1, a1);
+    if (it + 2 >= n_it) break;
+    count(x2, a2);
+    load(x2, a2);
   }
   if constexpr (!GLOBAL) {
     if (bulk) {

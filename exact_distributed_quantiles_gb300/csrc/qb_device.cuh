@@ -111,6 +111,21 @@ __device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+// Cluster barrier in two halves: every thread of every CTA of the cluster
+// arrives, and waits until all have arrived.  arrive_relaxed orders nothing
+// (it only records that the CTA is running); arrive_release makes this
+// thread's earlier writes, distributed shared memory included, visible to
+// the threads that then pass wait.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // round toward zero (used to truncate by adding 2^23)
 __device__ __forceinline__ f2_t f2_add_rz(f2_t a, f2_t b) {
   f2_t d;

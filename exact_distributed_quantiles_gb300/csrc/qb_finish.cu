@@ -190,12 +190,12 @@ __global__ void __launch_bounds__(256) select_hi_kernel(const int32_t* __restric
 //   mu = (sum_j q_j in fp64) / E.  A bf16 number is m * 2^(e - 134) with an
 //   8-bit m (e the biased exponent, 1 for subnormals), so when the non-zero
 //   q_j's exponents span at most 36 (none inf or NaN) the sum is the integer
-//   S = sum_j +-m_j * 2^(e_j - e_min) < 2^53 times 2^(e_min - 134): every CTA
-//   sends its partial integer sum (relative to its own e_min) with its
-//   exponent range in one cluster exchange, and mu = S * 2^(e_min - 134) / E
-//   is exact -- the value of the ascending serial fp64 sum, which is then
-//   exact too.  Otherwise every CTA sums all E values serially in ascending
-//   j in fp64, read over distributed shared memory;
+//   S = sum_j +-m_j * 2^(e_j - e_min) < 2^53 times 2^(e_min - 134), and
+//   mu = S * 2^(e_min - 134) / E is exact -- the value of the ascending
+//   serial fp64 sum, which is then exact too.  Otherwise the ascending
+//   serial fp64 sum is taken.  Every CTA writes its q_j into every CTA's
+//   shared memory (one cluster barrier), so each derives mu from all E
+//   values by itself, the same way;
 //   bias_out[j] = RN32(q_j - mu).
 // ------------------------------------------------------------------------
 constexpr int kFinCluster = 8;
@@ -214,10 +214,12 @@ __global__ void __cluster_dims__(kFinCluster, 1, 1) __launch_bounds__(kFinThread
                         int reset) {
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
-  __shared__ float q_s[64];
-  __shared__ int emin_s, emax_s, bad_s;
-  __shared__ long long part_s;
+  __shared__ float q_s[64];                   // this CTA's quantiles
+  __shared__ float q_all[64 * kFinCluster];   // every CTA's, pushed by their owners
   __shared__ double mu_s;
+  // this CTA is running: other CTAs may write into its shared memory once
+  // the matching wait has passed
+  cluster_arrive_relaxed();
   const int per = E / kFinCluster;  // experts of this CTA (4 .. 64)
   const int j0 = rank * per;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -274,84 +276,65 @@ __global__ void __cluster_dims__(kFinCluster, 1, 1) __launch_bounds__(kFinThread
     }
   }
   __syncthreads();
+  // every CTA has started: push this CTA's quantiles into every CTA, then
+  // one cluster barrier makes them visible everywhere
+  cluster_wait();
+  for (int t = threadIdx.x; t < per * kFinCluster; t += kFinThreads) {
+    const int c = t / per, jl = t - c * per;
+    *cluster.map_shared_rank(q_all + j0 + jl, c) = q_s[jl];
+  }
+  cluster_arrive_release();
+  cluster_wait();
+  // every CTA derives the same mean from all E quantiles
   if (warp == 0) {
-    // this CTA's exponent range and integer partial sum (relative to its e_min)
-    uint32_t u[2];
-    int ex[2], nz[2];
+    uint32_t u[16];
+    int bad = 0, emin = kNoExp, emax = -kNoExp;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int jl = lane + 32 * h;
-      u[h] = jl < per ? __float_as_uint(q_s[jl]) : 0u;
-      ex[h] = (int)((u[h] >> 23) & 0xFFu);
-      nz[h] = (u[h] & 0x7FFFFFFFu) != 0;
+    for (int h = 0; h < 16; ++h) {
+      const int j = lane + 32 * h;
+      u[h] = j < E ? __float_as_uint(q_all[j]) : 0u;
+      const int ex = (int)((u[h] >> 23) & 0xFFu);
+      bad |= ex == 0xFF;
+      if (u[h] & 0x7FFFFFFFu) {
+        emin = min(emin, ex);
+        emax = max(emax, ex);
+      }
     }
-    const int bad = __reduce_or_sync(0xffffffffu, (ex[0] == 0xFF) | (ex[1] == 0xFF));
-    const int emin = (int)__reduce_min_sync(0xffffffffu, (unsigned)min(nz[0] ? ex[0] : kNoExp,
-                                                                         nz[1] ? ex[1] : kNoExp));
-    const int emax = __reduce_max_sync(0xffffffffu, max(nz[0] ? ex[0] : -kNoExp,
-                                                        nz[1] ? ex[1] : -kNoExp));
-    long long part = 0;
-    if (!bad && emin != kNoExp && emax - emin <= 36) {
+    bad = __reduce_or_sync(0xffffffffu, bad);
+    emin = (int)__reduce_min_sync(0xffffffffu, (unsigned)emin);
+    emax = __reduce_max_sync(0xffffffffu, emax);
+    double mu;
+    if (!bad && emin == kNoExp) {
+      mu = 0.0;  // every q_j is zero
+    } else if (!bad && emax - emin <= 36) {
       const int base_e = max(emin, 1);
+      long long S = 0;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (nz[h]) {
-          const int e_eff = max(ex[h], 1);
-          const long long m = (long long)(((u[h] >> 16) & 0x7Fu) | (ex[h] ? 0x80u : 0u));
-          const long long term = m << (e_eff - base_e);
-          part += (u[h] >> 31) ? -term : term;
+      for (int h = 0; h < 16; ++h) {
+        if (u[h] & 0x7FFFFFFFu) {
+          const int ex = (int)((u[h] >> 23) & 0xFFu);
+          const long long m = (long long)(((u[h] >> 16) & 0x7Fu) | (ex ? 0x80u : 0u));
+          const long long term = m << (max(ex, 1) - base_e);
+          S += (u[h] >> 31) ? -term : term;
         }
       }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-    }
-    if (lane == 0) {
-      emin_s = emin;
-      emax_s = emax;
-      bad_s = bad;
-      part_s = part;
-    }
-  }
-  cluster.sync();
-  if (threadIdx.x == 0) {
-    int gmin = kNoExp, gmax = -kNoExp, gbad = 0;
-    int emin_r[kFinCluster];
-    long long part_r[kFinCluster];
-#pragma unroll
-    for (int r = 0; r < kFinCluster; ++r) {
-      emin_r[r] = *cluster.map_shared_rank(&emin_s, r);
-      part_r[r] = *cluster.map_shared_rank(&part_s, r);
-      gmin = min(gmin, emin_r[r]);
-      gmax = max(gmax, *cluster.map_shared_rank(&emax_s, r));
-      gbad |= *cluster.map_shared_rank(&bad_s, r);
-    }
-    double mu;
-    if (gbad == 0 && gmin == kNoExp) {
-      mu = 0.0;  // every q_j is zero
-    } else if (gbad == 0 && gmax - gmin <= 36) {
-      const int g_e = max(gmin, 1);
-      long long S = 0;
-#pragma unroll
-      for (int r = 0; r < kFinCluster; ++r)
-        if (emin_r[r] != kNoExp) S += part_r[r] << (max(emin_r[r], 1) - g_e);
-      // 2^(g_e - 134 - log2 E) as a double (a normal number for every g_e)
-      const double scale = __longlong_as_double((long long)(g_e - 134 - log2E + 1023) << 52);
+      for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+      // 2^(base_e - 134 - log2 E) as a double (a normal number for every base_e)
+      const double scale = __longlong_as_double((long long)(base_e - 134 - log2E + 1023) << 52);
       mu = __dmul_rn((double)S, scale);
     } else {
       double sum = 0.0;
-      for (int r = 0; r < kFinCluster; ++r) {
-        const float* qr = cluster.map_shared_rank(q_s, r);
-        for (int jl = 0; jl < per; ++jl) sum = __dadd_rn(sum, (double)qr[jl]);
-      }
+      if (lane == 0)
+        for (int j = 0; j < E; ++j) sum = __dadd_rn(sum, (double)q_all[j]);
       mu = __ddiv_rn(sum, (double)E);
     }
-    mu_s = mu;
+    if (lane == 0) mu_s = mu;
   }
   __syncthreads();
   const double mu = mu_s;
   for (int jl = threadIdx.x; jl < per; jl += kFinThreads)
     bias_out[j0 + jl] = __double2float_rn(__dsub_rn((double)q_s[jl], mu));
-  cluster.sync();  // keep every CTA's shared memory alive until the others have read it
 }
 
 // ------------------------------------------------------------------------

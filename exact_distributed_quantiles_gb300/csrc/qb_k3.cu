@@ -21,10 +21,11 @@
 // are added to the global histogram once per CTA.
 //
 // Finalize.  One cluster of 8 CTAs: a warp per expert finds the bin (blocks
-// of 128 bins, coalesced loads, a warp scan per block), the
-// fp64 quantiles are summed per CTA and the 8 partial sums are combined
-// through distributed shared memory in rank order, so every CTA derives the
-// same mean; min and max of the new bias go through the cluster the same way.
+// of 128 bins, coalesced loads, a warp scan per block) and resets the row;
+// each CTA then writes its fp64 quantiles into every CTA's shared memory
+// (one cluster barrier), so that every CTA holds all E of them and derives
+// the same mean -- per-CTA partial sums by a fixed shuffle tree, added in
+// rank order -- and rank 0 the min and max of the new bias for the bounds.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
@@ -305,10 +306,14 @@ __global__ void __cluster_dims__(kFinCluster, 1, 1) __launch_bounds__(kFinThread
                        float* __restrict__ bounds, float* __restrict__ bias_out, int reset) {
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
-  __shared__ double q_s[64];
-  __shared__ float b_s[64];
-  __shared__ double part_s;
-  __shared__ float min_s, max_s;
+  __shared__ double q_s[64];          // this CTA's quantiles
+  __shared__ double q_all[64 * kFinCluster];  // every CTA's, pushed by their owners
+  __shared__ double part_s[kFinCluster];
+  __shared__ float mn_s[32], mx_s[32];
+  __shared__ double mu_s;
+  // (1) this CTA is running: other CTAs may write into its shared memory
+  // once the matching wait has passed
+  cluster_arrive_relaxed();
   const int per = E / kFinCluster;  // experts of this CTA (4 .. 64)
   const int j0 = rank * per;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -319,6 +324,7 @@ __global__ void __cluster_dims__(kFinCluster, 1, 1) __launch_bounds__(kFinThread
   // is an fp32 quotient; either differs from the divided form by far less
   // than the mode's tolerance (the fraction is scaled by width, ~1e-3).
   const double width = __dmul_rn(__dsub_rn((double)hi, dlo), inv_nbins);
+  const bool vec = (nbins % 4 == 0) && (reinterpret_cast<uintptr_t>(hist) % 16 == 0);
   for (int jl = warp; jl < per; jl += kFinThreads / 32) {
     int32_t* row = hist + (int64_t)(j0 + jl) * nbins;
     long long before = 0;
@@ -333,58 +339,78 @@ __global__ void __cluster_dims__(kFinCluster, 1, 1) __launch_bounds__(kFinThread
       }
     }
     __syncwarp();
-    if (reset)
-      for (int i = lane; i < nbins; i += 32) row[i] = 0;
+    if (reset) {
+      if (vec) {
+        int4* row4 = reinterpret_cast<int4*>(row);
+        for (int i = lane; i < nbins / 4; i += 32) row4[i] = make_int4(0, 0, 0, 0);
+      } else {
+        for (int i = lane; i < nbins; i += 32) row[i] = 0;
+      }
+    }
   }
   __syncthreads();
-  if (warp == 0) {
-    double v = lane < per ? q_s[lane] : 0.0;
-    if (lane + 32 < per) v = __dadd_rn(v, q_s[lane + 32]);
+  // (2) every CTA has started: push this CTA's quantiles into every CTA
+  cluster_wait();
+  for (int t = threadIdx.x; t < per * kFinCluster; t += kFinThreads) {
+    const int c = t / per, jl = t - c * per;
+    *cluster.map_shared_rank(q_all + j0 + jl, c) = q_s[jl];
+  }
+  cluster_arrive_release();
+  cluster_wait();
+  // (3) every CTA now holds all E quantiles and derives the same mean: the
+  // per-CTA partial sums (a shuffle tree over each CTA's experts), added in
+  // rank order
+  if (warp < kFinCluster) {
+    const double* qc = q_all + warp * per;
+    double v = lane < per ? qc[lane] : 0.0;
+    if (lane + 32 < per) v = __dadd_rn(v, qc[lane + 32]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = __dadd_rn(v, __shfl_down_sync(0xffffffffu, v, o));
-    if (lane == 0) part_s = v;
-  }
-  cluster.sync();
-  // every CTA adds the eight partial sums in rank order: the same mean everywhere
-  double sum = 0.0;
-#pragma unroll
-  for (int c = 0; c < kFinCluster; ++c) sum = __dadd_rn(sum, *cluster.map_shared_rank(&part_s, c));
-  const double mu = __dmul_rn(sum, 1.0 / (double)E);  // E is a power of two: exact
-  for (int jl = threadIdx.x; jl < per; jl += kFinThreads) {
-    const float b = __double2float_rn(__dsub_rn(q_s[jl], mu));
-    b_s[jl] = b;
-    bias_out[j0 + jl] = b;
+    if (lane == 0) part_s[warp] = v;
   }
   __syncthreads();
-  if (warp == 0) {
-    float mn = lane < per ? b_s[lane] : INFINITY;
-    float mx = lane < per ? b_s[lane] : -INFINITY;
-    if (lane + 32 < per) {
-      mn = fminf(mn, b_s[lane + 32]);
-      mx = fmaxf(mx, b_s[lane + 32]);
-    }
+  if (threadIdx.x == 0) {
+    double sum = 0.0;
+#pragma unroll
+    for (int c = 0; c < kFinCluster; ++c) sum = __dadd_rn(sum, part_s[c]);
+    mu_s = __dmul_rn(sum, 1.0 / (double)E);  // E is a power of two: exact
+  }
+  __syncthreads();
+  const double mu = mu_s;
+  // every new bias (this CTA writes its own), and their min and max for the
+  // next bounds (rank 0 writes them; every CTA read the old ones above)
+  float mn = INFINITY, mx = -INFINITY;
+  for (int j = threadIdx.x; j < E; j += kFinThreads) {
+    const float b = __double2float_rn(__dsub_rn(q_all[j], mu));
+    if (j >= j0 && j < j0 + per) bias_out[j] = b;
+    mn = fminf(mn, b);
+    mx = fmaxf(mx, b);
+  }
+  if (rank == 0) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     }
     if (lane == 0) {
-      min_s = mn;
-      max_s = mx;
+      mn_s[warp] = mn;
+      mx_s[warp] = mx;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      mn = mn_s[lane];
+      mx = mx_s[lane];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      }
+      if (lane == 0) {
+        bounds[0] = __fsub_rn(mn, 1.0f);
+        bounds[1] = __fadd_rn(mx, 1.0f);
+      }
     }
   }
-  // every CTA has read the old bounds (above) before rank 0 writes new ones
-  cluster.sync();
-  if (rank == 0 && threadIdx.x == 0) {
-    float mn = min_s, mx = max_s;
-    for (int c = 1; c < kFinCluster; ++c) {
-      mn = fminf(mn, *cluster.map_shared_rank(&min_s, c));
-      mx = fmaxf(mx, *cluster.map_shared_rank(&max_s, c));
-    }
-    bounds[0] = __fsub_rn(mn, 1.0f);
-    bounds[1] = __fadd_rn(mx, 1.0f);
-  }
-  cluster.sync();  // keep every CTA's shared memory alive until rank 0 has read it
 }
 
 }  // namespace

@@ -704,12 +704,37 @@ __global__ void __launch_bounds__(warps_max(MODE) * 32, 1) route256_kernel(const
 
   // ---- flush the shared window: one global atomic per non-zero counter
   if constexpr (MODE == kHi256) {
-    __syncthreads();
-    for (int w = threadIdx.x; w < kWin * kE; w += blockDim.x) {
-      const int cnt = hist_s[w];
-      if (cnt) {
-        const int slot = w >> 8, p = w & 255;
-        atomicAdd(a.hist + (int64_t)expert_of(p & 31, p >> 5) * 256 + slot_bin(slot), cnt);
+    const int nw = (int)(blockDim.x >> 5);
+    if (nw * kWarpBytes >= kE * (kWin + 1) * 4) {
+      // Coalesced: the window is first transposed into the (now idle) tile
+      // buffers as rows r = 32 i + L (expert expert_of(L, i)) of 33 words, so
+      // that a warp then adds one expert's 32 slots -- two runs of 16
+      // consecutive words of its histogram row (hi bytes 0xB0-0xBF and
+      // 0x40-0x4F) -- instead of 32 counters of 32 different experts.  Both
+      // copies are conflict-free: word (r, slot) sits in bank (r + slot) % 32.
+      // Every lane first waits for its own row copies (after a timed-out
+      // wait some may still be landing in those buffers).
+      asm volatile("cp.async.wait_all;" ::: "memory");
+      __syncthreads();
+      int32_t* stg = reinterpret_cast<int32_t*>(smem + hist_bytes(MODE));
+      for (int p = warp; p < kWin * 8; p += nw) {
+        const int i = p & 7, slot = p >> 3;
+        stg[(32 * i + lane) * (kWin + 1) + slot] = hist_s[lane + 32 * i + 256 * slot];
+      }
+      __syncthreads();
+      for (int r = warp; r < kE; r += nw) {
+        const int cnt = stg[r * (kWin + 1) + lane];
+        if (cnt)
+          atomicAdd(a.hist + (int64_t)expert_of(r & 31, r >> 5) * 256 + slot_bin(lane), cnt);
+      }
+    } else {
+      __syncthreads();
+      for (int w = threadIdx.x; w < kWin * kE; w += blockDim.x) {
+        const int cnt = hist_s[w];
+        if (cnt) {
+          const int slot = w >> 8, p = w & 255;
+          atomicAdd(a.hist + (int64_t)expert_of(p & 31, p >> 5) * 256 + slot_bin(slot), cnt);
+        }
       }
     }
   }

@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(kCountThreads, 1)
   // counter address of bin pattern u for element i: hb + 4 (i pitch) + 4 (u - 0x4B000000)
   const uint32_t hb0 = hb - 4u * 0x4B000000u;
   // Three row buffers used in turn (the compiler keeps them in registers
-  // without copies): row rc is counted from one while the next two rows'
+  // without copies): a row is counted from one while the next two rows'
   // loads are in flight, and the freed buffer loads the row three strides on.
   float x0[8], x1[8], x2[8];
   float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f;
@@ -123,14 +123,23 @@ __global__ void __launch_bounds__(kCountThreads, 1)
   for (int i = 0; i < 8; ++i) x0[i] = x1[i] = x2[i] = 0.0f;
   const int64_t w0 = r_begin + warp * 8;   // this warp's first row
   const int64_t n_it = w0 < r_end ? (r_end - w0 + stride - 1) / stride : 0;
-  int64_t rc = w0 + rsub;                  // row counted next (this lane)
-  int64_t rl = rc;                         // row loaded next (this lane)
+  // this lane's rows are w0 + rsub + j * stride, j = 0, 1, ...: n_mine of them
+  // are in range; the loads and the counts each walk them with a pointer
+  // and a countdown
+  const int64_t r_mine = w0 + rsub;
+  const int n_mine = r_mine < r_end ? (int)((r_end - 1 - r_mine) / stride) + 1 : 0;
+  const T* pl = base + r_mine * E;
+  const float* pa = alpha + r_mine;
+  const int64_t step_l = stride * E;
+  int left_l = n_mine, left_c = n_mine;
   auto load = [&](float (&x)[8], float& a) {
-    if (rl < r_end) {
-      load8x(base + rl * E, x);
-      a = __ldg(alpha + rl);
+    if (left_l > 0) {
+      load8x(pl, x);
+      a = __ldg(pa);
     }
-    rl += stride;
+    --left_l;
+    pl += step_l;
+    pa += stride;
   };
   auto count = [&](const float (&x)[8], float a) {
     float m = 0.0f;
@@ -153,7 +162,7 @@ __global__ void __launch_bounds__(kCountThreads, 1)
       const f2_t R = f2_add(A, f2_pack(sn[2 * i], sn[2 * i + 1]));
       f2_unpack(f2_add_rz(f2_mul(f2_sub(R, LO), SC), M23), u[2 * i], u[2 * i + 1]);
     }
-    if (rc < r_end) {
+    if (left_c > 0) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const uint32_t ub = __float_as_uint(fminf(fmaxf(u[i], 8388608.0f), u_last));
@@ -163,7 +172,7 @@ __global__ void __launch_bounds__(kCountThreads, 1)
           red_shared_inc(hb0 + 4u * (uint32_t)(i * pitch) + 4u * ub);
       }
     }
-    rc += stride;
+    --left_c;
   };
   load(x0, a0);
   load(x1, a1);

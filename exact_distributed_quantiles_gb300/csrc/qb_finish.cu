@@ -190,10 +190,10 @@ __global__ void __launch_bounds__(256) select_hi_kernel(const int32_t* __restric
 //   mu = (sum_j q_j in fp64) / E.  A bf16 number is m * 2^(e - 134) with an
 //   8-bit m (e the biased exponent, 1 for subnormals), so when the non-zero
 //   q_j's exponents span at most 36 (none inf or NaN) the sum is the integer
-//   S = sum_j +-m_j * 2^(e_j - e_min) < 2^53 times 2^(e_min - 134), and
-//   mu = S * 2^(e_min - 134) / E is exact -- the value of the ascending
-//   serial fp64 sum, which is then exact too.  Otherwise the ascending
-//   serial fp64 sum is taken.  Every CTA writes its q_j into every CTA's
+//   S = sum_j +-m_j * 2^(e_j - e_min) < 2^53 times 2^(e_min - 134), the
+//   exact value of the ascending serial fp64 sum (which is then exact too),
+//   and mu = RN(S * 2^(e_min - 134) / E) (a product by 2^-log2(E) when E is
+//   a power of two).  Otherwise the ascending serial fp64 sum is taken.  Every CTA writes its q_j into every CTA's
 //   shared memory (one cluster barrier), so each derives mu from all E
 //   values by itself, the same way;
 //   bias_out[j] = RN32(q_j - mu).
@@ -320,9 +320,15 @@ __global__ void __cluster_dims__(kFinCluster, 1, 1) __launch_bounds__(kFinThread
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
-      // 2^(base_e - 134 - log2 E) as a double (a normal number for every base_e)
-      const double scale = __longlong_as_double((long long)(base_e - 134 - log2E + 1023) << 52);
-      mu = __dmul_rn((double)S, scale);
+      if (log2E >= 0) {
+        // 2^(base_e - 134 - log2 E) as a double (a normal number for every base_e)
+        const double scale = __longlong_as_double((long long)(base_e - 134 - log2E + 1023) << 52);
+        mu = __dmul_rn((double)S, scale);
+      } else {
+        // the exact sum S * 2^(base_e - 134) (a normal double), divided once
+        const double scale = __longlong_as_double((long long)(base_e - 134 + 1023) << 52);
+        mu = __ddiv_rn(__dmul_rn((double)S, scale), (double)E);
+      }
     } else {
       double sum = 0.0;
       if (lane == 0)
@@ -465,7 +471,8 @@ int launch_finalize(int32_t* hist_hi, int32_t* hist_lo, const int32_t* sel, cons
                     int E, float* bias_out, uint16_t* qkey_out, int reset, cudaStream_t stream) {
   if (E % kFinCluster != 0 || E / kFinCluster > 64) return QB_EUNSUPPORTED;
   int log2E = 0;
-  while ((1 << log2E) < E) ++log2E;  // E is a power of two
+  while ((1 << log2E) < E) ++log2E;
+  if ((1 << log2E) != E) log2E = -1;  // not a power of two: the mean divides
   eqb_finalize_kernel<<<kFinCluster, kFinThreads, 0, stream>>>(hist_hi, hist_lo, sel, r_lo, E, log2E,
                                                                bias_out, qkey_out, reset);
   return launch_status();

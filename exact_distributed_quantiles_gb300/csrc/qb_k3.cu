@@ -382,7 +382,8 @@ __global__ void __cluster_dims__(kFinCluster, 1, 1) __launch_bounds__(kFinThread
     double sum = 0.0;
 #pragma unroll
     for (int c = 0; c < kFinCluster; ++c) sum = __dadd_rn(sum, part_s[c]);
-    mu_s = __dmul_rn(sum, 1.0 / (double)E);  // E is a power of two: exact
+    // E a power of two: the product is the quotient; otherwise divide
+    mu_s = (E & (E - 1)) == 0 ? __dmul_rn(sum, 1.0 / (double)E) : __ddiv_rn(sum, (double)E);
   }
   __syncthreads();
   const double mu = mu_s;

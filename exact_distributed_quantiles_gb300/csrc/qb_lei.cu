@@ -229,10 +229,10 @@ constexpr int kApplyU = 8;
 constexpr int kApplyIters = 4;
 
 __global__ void __launch_bounds__(kApplyThreads, 7)
-    lei_apply_kernel(float* __restrict__ grad, int N, int e4_log2, int batch_tokens,
+    lei_apply_kernel(float* __restrict__ grad, int N, int e4, int lanes_log2, int batch_tokens,
                      const float* __restrict__ ws) {
-  const int e4 = 1 << e4_log2;  // 16-byte chunks per row
-  const int lanes_log2 = e4_log2 < 7 ? e4_log2 : 7;  // lanes per row: min(e4, 128)
+  // e4 16-byte chunks per row; 2^lanes_log2 lanes per row (<= e4, <= 128),
+  // each taking the row's chunks col, col + lanes, ...
   const int lanes_per_row = 1 << lanes_log2;
   const int rows_per_pass = kApplyThreads >> lanes_log2;
   const int r_in = threadIdx.x >> lanes_log2;
@@ -251,20 +251,20 @@ __global__ void __launch_bounds__(kApplyThreads, 7)
 #pragma unroll
       for (int u = 0; u < kApplyU; ++u) {
         const int rr = r0 + u * rows_per_pass + r_in;
-        if (rr <= last) g[u] = __ldcs(g4 + ((int64_t)rr << e4_log2) + col);
+        if (rr <= last) g[u] = __ldcs(g4 + (int64_t)rr * e4 + col);
       }
-      float4 c = __ldg(c4 + ((int64_t)b0 << e4_log2) + col);
+      float4 c = __ldg(c4 + (int64_t)b0 * e4 + col);
 #pragma unroll
       for (int u = 0; u < kApplyU; ++u) {
         const int rr = r0 + u * rows_per_pass + r_in;
         if (rr <= last) {
-          if (!one_batch) c = __ldg(c4 + ((int64_t)(rr / batch_tokens) << e4_log2) + col);
+          if (!one_batch) c = __ldg(c4 + (int64_t)(rr / batch_tokens) * e4 + col);
           float4 o;
           o.x = __fadd_rn(g[u].x, c.x);
           o.y = __fadd_rn(g[u].y, c.y);
           o.z = __fadd_rn(g[u].z, c.z);
           o.w = __fadd_rn(g[u].w, c.w);
-          __stcs(g4 + ((int64_t)rr << e4_log2) + col, o);
+          __stcs(g4 + (int64_t)rr * e4 + col, o);
         }
       }
     }
@@ -293,6 +293,7 @@ __global__ void __maxnreg__(32) lei_apply_bulk_kernel(float* __restrict__ grad, 
   const int lane = threadIdx.x;
   const int rep = kBulkBytes / (E * 4);  // rows per bulk op (E <= 512: at least 2)
   const int e4 = E >> 2;
+  const int fill = rep * e4;             // 16-byte chunks of the block in use
   const int64_t groups = ((int64_t)N + rep - 1) / rep;
   const int64_t g0 = groups * blockIdx.x / gridDim.x;
   const int64_t g1 = groups * (blockIdx.x + 1) / gridDim.x;
@@ -307,7 +308,7 @@ __global__ void __maxnreg__(32) lei_apply_bulk_kernel(float* __restrict__ grad, 
     __syncwarp();
     const float4* c4 = reinterpret_cast<const float4*>(ws + b * E);
     float4* b4 = reinterpret_cast<float4*>(buf);
-    for (int i = lane; i < kBulkBytes / 16; i += 32) b4[i] = __ldg(c4 + (i & (e4 - 1)));
+    for (int i = lane; i < fill; i += 32) b4[i] = __ldg(c4 + i % e4);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     if (lane == 0) {
@@ -353,12 +354,12 @@ int launch_lei_rho(const int32_t* topk, int64_t N, int E, int k, float eta,
 
 int launch_lei_apply(float* grad, int64_t N, int E, int64_t batch_tokens, const float* workspace,
                      cudaStream_t stream) {
-  int e4_log2 = 0;
-  while ((1 << e4_log2) < E / 4) ++e4_log2;  // E is a power of two
-  const int lanes_log2 = e4_log2 < 7 ? e4_log2 : 7;
+  const int e4 = E / 4;
+  int lanes_log2 = 0;  // the largest power of two <= min(e4, 128)
+  while (lanes_log2 < 7 && (2 << lanes_log2) <= e4) ++lanes_log2;
   const int64_t cta_rows = (int64_t)(kApplyThreads >> lanes_log2) * kApplyU * kApplyIters;
   const int64_t grid = (N + cta_rows - 1) / cta_rows;
-  lei_apply_kernel<<<(unsigned)grid, kApplyThreads, 0, stream>>>(grad, (int)N, e4_log2,
+  lei_apply_kernel<<<(unsigned)grid, kApplyThreads, 0, stream>>>(grad, (int)N, e4, lanes_log2,
                                                                 (int)batch_tokens, workspace);
   return launch_status();
 }

@@ -65,6 +65,12 @@ struct Args {
   const float* bounds;  // k3 mode
   int nbins;            // k3 mode
   int* status;
+  // Experts per row in memory (logits, bias, keys, sel, top-k indices).  The
+  // kernel's tile geometry is for E (a power of two); a call with
+  // e_real < E (any multiple of 32) pads each row in shared memory: the
+  // padded experts get bias -inf and score 0, so v = -inf keeps them out of
+  // the top-(k+1), and nothing of theirs is stored or counted.
+  int e_real;
 };
 
 template <int E, int TILE>
@@ -237,11 +243,18 @@ __device__ __forceinline__ int rows_free(int F) {
 
 template <int E, typename T, int TILE>
 __device__ __forceinline__ void issue_rows(unsigned char* tile, const T* logits, int64_t tile_start,
-                                           int r0, int r1, uint64_t* bar) {
+                                           int r0, int r1, int er, uint64_t* bar) {
   if (r1 <= r0) return;
   fence_proxy_async_smem();
-  bulk_g2s(x_ptr<E, T, TILE>(tile, r0 * E), logits + (tile_start + r0) * (int64_t)E,
-           (uint32_t)((r1 - r0) * E * sizeof(T)), bar);
+  if (er == E) {
+    bulk_g2s(x_ptr<E, T, TILE>(tile, r0 * E), logits + (tile_start + r0) * (int64_t)E,
+             (uint32_t)((r1 - r0) * E * sizeof(T)), bar);
+  } else {
+    // padded rows: one copy of the er experts of each row
+    for (int r = r0; r < r1; ++r)
+      bulk_g2s(x_ptr<E, T, TILE>(tile, r * E), logits + (tile_start + r) * (int64_t)er,
+               (uint32_t)(er * sizeof(T)), bar);
+  }
 }
 
 // Issue the load of every row group of the next tile that is complete inside
@@ -251,14 +264,14 @@ template <int E, typename T, int TILE, int GR>
 // uniform); only the leader lane issues the barrier arrival and the copy.
 __device__ __forceinline__ void issue_groups(unsigned char* tile, const T* logits, int64_t start,
                                              int nrows, int nf, int& issued, uint64_t* bars,
-                                             bool leader) {
+                                             bool leader, int er) {
   while (issued * GR < nrows) {
     const int r0 = issued * GR;
     const int r1 = (r0 + GR < nrows) ? r0 + GR : nrows;
     if (nf < r1) break;
     if (leader) {
-      mbar_arrive_expect_tx(bars + issued, (uint32_t)((r1 - r0) * E * sizeof(T)));
-      issue_rows<E, T, TILE>(tile, logits, start, r0, r1, bars + issued);
+      mbar_arrive_expect_tx(bars + issued, (uint32_t)((r1 - r0) * er * sizeof(T)));
+      issue_rows<E, T, TILE>(tile, logits, start, r0, r1, er, bars + issued);
     }
     ++issued;
   }
@@ -343,13 +356,14 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
   uint64_t* bars = reinterpret_cast<uint64_t*>(wbase + SM::kTileBytes + SM::kGmax + SM::kAlpha);
   const T* logits = static_cast<const T*>(a.logits);
   const int k = a.k;
+  const int er = a.e_real;  // experts per row in memory (<= E)
 
   // ---- prologue: zero the shared histogram, slot table, bias, barrier
   if constexpr (MODE == kModeHi) {
     for (int i = threadIdx.x; i < GE::NCOPY * GE::CSTRIDE; i += blockDim.x) hist_s[i] = 0;
     for (int i = threadIdx.x; i < 256; i += blockDim.x) lut[i] = (uint8_t)window_slot_of(i);
   }
-  for (int i = threadIdx.x; i < E; i += blockDim.x) bias_s[i] = a.bias[i];
+  for (int i = threadIdx.x; i < E; i += blockDim.x) bias_s[i] = i < er ? a.bias[i] : -INFINITY;
   if (lane == 0) {
     for (int q = 0; q < SM::NGRP; ++q) mbar_init(bars + q, 1);
     fence_mbar_init();
@@ -364,7 +378,7 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
   for (int i = 0; i < GE::BREG; ++i) {
     const int e = e0l + (i >> 3) * 256 + (i & 7);
     breg[i] = bias_s[e];
-    selreg[i] = (MODE == kModeLo) ? a.sel[e] : 0;
+    selreg[i] = (MODE == kModeLo && e < er) ? a.sel[e] : -1;
   }
   // shared byte address of this lane's counter for element i, slot 0
   const int copy = (E >= 256) ? 0 : (8 * lane) / E;
@@ -380,7 +394,7 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
     const int64_t t0 = tix * TILE;
     const int rows = (int)((a.N - t0) < TILE ? (a.N - t0) : TILE);
     int issued = 0;
-    issue_groups<E, T, TILE, GR>(tile, logits, t0, rows, rows, issued, bars, true);
+    issue_groups<E, T, TILE, GR>(tile, logits, t0, rows, rows, issued, bars, true, er);
   }
 
   for (; tix < n_tiles && ok; tix += wstride) {
@@ -438,6 +452,11 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
         if (!act[u]) continue;
         const int st = st0 + u;
         const int f = st * 256 + 8 * lane;
+        if (er < E && (f % E) >= er) {
+          // a padded expert: score 0 (its logit slot holds stale bytes), v = -inf
+#pragma unroll
+          for (int i = 0; i < 8; ++i) s[u][i] = 0.0f;
+        }
         const bool hi = (E == 512) && (st & 1);
         float v[8];
 #pragma unroll
@@ -673,16 +692,18 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
       const int e0 = f % E;
       const bool act = row < rows;
       const int64_t tok = t0 + row;
+      const bool real = e0 < er;  // not a padded expert
       if constexpr (MODE == kModeK3) {
         // alpha only (phase B wrote it): the K3 counts are taken by the
         // counting kernel from the logits and alpha
         (void)tok;
         (void)e0;
         (void)act;
+        (void)real;
       } else {
         uint32_t kw[4] = {0u, 0u, 0u, 0u};
         bool out_of_window = false;
-        if (act) {
+        if (act && real) {
           float s[8];
           load8(sc + f, s);
           if (tile_ext)
@@ -690,7 +711,7 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
           else
             keys8<false>(alpha_s[row], s, kw);
           if (MODE == kModeHi && a.keys_out)
-            *reinterpret_cast<uint4*>(a.keys_out + tok * E + e0) =
+            *reinterpret_cast<uint4*>(a.keys_out + tok * er + e0) =
                 make_uint4(kw[0], kw[1], kw[2], kw[3]);
           if constexpr (MODE == kModeHi) {
             const uint32_t hoff = (E == 512 && (st & 1)) ? 1024u : 0u;  // +256 experts
@@ -728,7 +749,7 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
       __syncwarp();
       if (nrows > 0)
         issue_groups<E, T, TILE, GR>(tile, logits, n0, nrows, rows_free<E, T, TILE>((st + 1) * 256),
-                                     issued, bars, lane == 0);
+                                     issued, bars, lane == 0, er);
     }
   }
 
@@ -798,10 +819,14 @@ int launch_mode(const void* logits, int dtype, const float* bias, int64_t N, int
                 int32_t* hist, uint16_t* keys_out, int32_t* topk_out, float* alpha_out,
                 const int32_t* sel, const float* bounds, int nbins, cudaStream_t stream) {
   Args a{logits, bias, N, k, hist, keys_out, topk_out, alpha_out, sel, bounds, nbins,
-         device_status_ptr()};
+         device_status_ptr(), E};
   if (!a.status) return QB_ECUDA;
-  if (dtype == QB_F32) return dispatch_E<MODE, float, QB_ROUTE_TILE>(E, k, a, stream);
-  return dispatch_E<MODE, __nv_bfloat16, QB_ROUTE_TILE>(E, k, a, stream);
+  // the tile geometry of the next power of two (a row of E = 96 sits in a
+  // 128-expert slot)
+  int ep = 32;
+  while (ep < E) ep <<= 1;
+  if (dtype == QB_F32) return dispatch_E<MODE, float, QB_ROUTE_TILE>(ep, k, a, stream);
+  return dispatch_E<MODE, __nv_bfloat16, QB_ROUTE_TILE>(ep, k, a, stream);
 }
 
 }  // namespace route

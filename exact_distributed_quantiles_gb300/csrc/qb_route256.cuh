@@ -801,7 +801,7 @@ template <typename T>
 int launch_hi_t(const void* logits, const float* bias, int64_t N, int k, int32_t* hist,
                 uint16_t* keys_out, int32_t* topk_out, float* alpha_out, cudaStream_t stream) {
   Args a{logits, bias, N, k, hist, keys_out, topk_out, alpha_out, nullptr, nullptr, 0,
-         device_status_ptr()};
+         device_status_ptr(), kE};
   if (!a.status) return QB_ECUDA;
   return dispatch_k<T, kHi256>(k, a, stream);
 }
@@ -811,7 +811,7 @@ template <typename T>
 int launch_alpha_t(const void* logits, const float* bias, int64_t N, int k, float* alpha_out,
                    cudaStream_t stream) {
   Args a{logits, bias, N, k, nullptr, nullptr, nullptr, alpha_out, nullptr, nullptr, 0,
-         device_status_ptr()};
+         device_status_ptr(), kE};
   if (!a.status) return QB_ECUDA;
   return dispatch_k<T, kAlpha256>(k, a, stream);
 }

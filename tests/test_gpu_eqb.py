@@ -35,7 +35,11 @@ def _logits(N, E, seed, dtype=torch.float32, std=1.0, off_std=0.5):
     return x.to(dtype).contiguous(), b
 
 
-@pytest.mark.parametrize("E", [32, 64, 128, 256, 512])
+# powers of two, and multiples of 32 that run padded to the next one
+ALL_E = [32, 64, 96, 128, 160, 256, 384, 480, 512]
+
+
+@pytest.mark.parametrize("E", ALL_E)
 @pytest.mark.parametrize("k", [1, 6, 8, 15])
 def test_route_small_shapes_fp32(qb, orc, E, k):
     if k >= E:
@@ -47,7 +51,7 @@ def test_route_small_shapes_fp32(qb, orc, E, k):
     assert np.array_equal(res["hist_hi"], orc.hist_hi(orc.keys(ref["margins"])))
 
 
-@pytest.mark.parametrize("E,k", [(64, 6), (256, 8), (512, 6)])
+@pytest.mark.parametrize("E,k", [(64, 6), (96, 6), (256, 8), (384, 8), (512, 6)])
 @pytest.mark.parametrize("N", [1, 31, 32, 33, 1000])
 def test_route_bf16_and_ragged(qb, orc, E, k, N):
     x, b = _logits(N, E, seed=N + E, dtype=torch.bfloat16, std=1.5, off_std=0.3)
@@ -205,7 +209,8 @@ def test_full_step_layer_at_bench_size(qb, orc, layer):
         assert np.array_equal(np_u16(res["keys"]), np.concatenate(ref["keys"]))
 
 
-@pytest.mark.parametrize("E,k", [(32, 1), (64, 6), (128, 8), (256, 6), (512, 15)])
+@pytest.mark.parametrize("E,k", [(32, 1), (64, 6), (96, 6), (128, 8), (160, 15), (256, 6),
+                                 (384, 8), (480, 6), (512, 15)])
 def test_eqb_all_expert_counts(qb, orc, E, k):
     # the whole EQB chain (hi pass, select, lo pass from keys, finalize) for
     # every supported expert count, several tiles and a ragged tail
@@ -233,7 +238,7 @@ def _lo_keys(N, E, seed):
     return keys, sel
 
 
-@pytest.mark.parametrize("E", [32, 64, 128, 256, 512])
+@pytest.mark.parametrize("E", ALL_E)
 @pytest.mark.parametrize("N", [1, 31, 4097])
 def test_keys_hist_lo_equals_definition(qb, orc, E, N):
     # The lo pass from stored keys equals the oracle's direct count on keys
@@ -255,7 +260,7 @@ def _keys_of(values):
     return np.where(b & 0x8000, b ^ 0xFFFF, b ^ 0x8000).astype(np.uint16)
 
 
-@pytest.mark.parametrize("E", [32, 64, 128, 256, 512])
+@pytest.mark.parametrize("E", ALL_E)
 @pytest.mark.parametrize("spread", ["narrow", "wide", "no_bin"])
 def test_finalize_on_built_histograms(qb, orc, E, spread):
     # qb_finalize against the plain definition on hand-built histograms: the
@@ -309,7 +314,7 @@ def test_finalize_on_built_histograms(qb, orc, E, spread):
     assert np.array_equal(got.view(np.int32), want.view(np.int32))
 
 
-@pytest.mark.parametrize("E", [32, 64, 128, 256, 512])
+@pytest.mark.parametrize("E", ALL_E)
 @pytest.mark.parametrize("k", [1, 6, 15])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_lo_pass_recomputed_all_shapes(qb, orc, E, k, dtype):

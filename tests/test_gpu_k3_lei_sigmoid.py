@@ -113,6 +113,8 @@ def test_k3_workload(qb, orc):
                                               (32, 1, 1000, torch.bfloat16),
                                               (128, 3, 1000, torch.float32),
                                               (64, 6, 8000, torch.float32),   # global counts
+                                              (96, 6, 1000, torch.bfloat16),  # padded rows
+                                              (384, 8, 1000, torch.float32),
                                               (32, 2, 1, torch.float32)])
 def test_k3_small_shapes(qb, orc, E, k, nbins, dtype):
     w = inputs.scaled(inputs.WORKLOADS["k3"], E=E, k=k, n_micro=3, n_tokens=32 * 5 + 3,
@@ -176,7 +178,8 @@ def test_lei_full_step_microbatches(qb, orc):
         assert np.max(np.abs(c_all[m] - w.eta * rho)) <= w.eta * 2e-6
 
 
-@pytest.mark.parametrize("N,E,k,bt", [(1, 32, 1, 0), (1000, 64, 6, 333), (4097, 512, 15, 1024)])
+@pytest.mark.parametrize("N,E,k,bt", [(1, 32, 1, 0), (1000, 64, 6, 333), (4097, 512, 15, 1024),
+                                      (3001, 96, 6, 1000), (2049, 384, 8, 512)])
 def test_lei_shapes_and_ragged_batches(qb, orc, N, E, k, bt):
     topk = inputs.random_topk(N, E, k, seed=N, device="cuda")
     topk[: N // 3] = torch.arange(k, dtype=torch.int32, device="cuda")  # imbalance
@@ -198,7 +201,8 @@ def test_lei_shapes_and_ragged_batches(qb, orc, N, E, k, bt):
 
 
 @pytest.mark.parametrize("N,E,k,bt", [(1, 32, 1, 0), (1000, 64, 6, 333), (4097, 512, 15, 1024),
-                                      (70001, 256, 6, 4099)])
+                                      (70001, 256, 6, 4099), (5003, 160, 6, 777),
+                                      (4099, 480, 15, 1000)])
 def test_lei_rho_then_apply_equals_inject(qb, orc, N, E, k, bt):
     # The two halves on one stream give lei_inject's result bit for bit;
     # lei_apply alone is grad + workspace[batch(row)] in binary32 for every
@@ -235,6 +239,7 @@ def test_lei_rho_then_apply_equals_inject(qb, orc, N, E, k, bt):
 
 
 @pytest.mark.parametrize("N,E,bt", [(1, 32, 0), (1000, 64, 333), (4097, 512, 1024),
+                                    (3001, 96, 1000), (2049, 384, 512),
                                     (70001, 256, 4099), (524288, 256, 32768)])
 def test_lei_apply_overlap_equals_apply(qb, N, E, bt):
     # The bulk-copy variant gives lei_apply's result bit for bit, alone and

@@ -42,17 +42,17 @@ METRIC = "QB routed tokens/s per layer (E=256,k=6, 2-pass EQB) on 1 GB300; % of 
 # launch (route256_kernel, keys written, no top-k output) on a 524288-token
 # layer, from an ncu capture of that launch.  Reported only while the
 # kernel's sources hash to the value they had when the counters were taken.
-ROUTE_TRAFFIC = {"sha1": "910d9336b697e91ebccedd1c6a3bc2d8ec8047dc", "tokens": 524288,
-                 "bytes": (537.027840 + 233.271552) * 1e6}
+ROUTE_TRAFFIC = {"sha1": "37b0fa45713acc5d2be305b4496375d502c67603", "tokens": 524288,
+                 "bytes": (537.009152 + 233.401600) * 1e6}
 ROUTE_SOURCES = ("qb_route256.cuh", "qb_route256_f32.cu", "qb_route.cuh", "qb_device.cuh")
 # Warp instructions of the same capture (smsp__inst_executed.sum), for the
 # issue-rate roofline of this issue-bound kernel; same hash guard.
-ROUTE_INSTR = {"tokens": 524288, "warp_instructions": 127793975}
+ROUTE_INSTR = {"tokens": 524288, "warp_instructions": 127551415}
 # Warp instructions (smsp__inst_executed.sum) of one K3 microbatch of 65536
 # bf16 tokens: the alpha pass (route256_kernel, K3 mode) plus the count
 # kernel, from an ncu capture of those launches; reported while the K3
 # sources hash to the value they had when it was taken.
-K3_INSTR = {"sha1": "616af97329b21f58e7272566bdea452cc836243f", "tokens": 65536,
+K3_INSTR = {"sha1": "2d08cafb6f2baa93ef762e2bb00206ca6c6ea2b6", "tokens": 65536,
             "warp_instructions": 13063568 + 13192792}
 K3_SOURCES = ("qb_route256.cuh", "qb_route256_bf16.cu", "qb_route.cuh", "qb_device.cuh",
               "qb_k3.cu")

@@ -705,7 +705,14 @@ __global__ void __launch_bounds__(warps_max(MODE) * 32, 1) route256_kernel(const
   // ---- flush the shared window: one global atomic per non-zero counter
   if constexpr (MODE == kHi256) {
     const int nw = (int)(blockDim.x >> 5);
-    if (nw * kWarpBytes >= kE * (kWin + 1) * 4) {
+    // The transposed flush costs each CTA two more barriers and a pass over
+    // the window in shared memory; it pays when the launch is long (many
+    // rounds of tiles: the scattered adds of 152 CTAs then contend in L2),
+    // not for a launch of a few rounds (a 32768-token microbatch: 2 rounds;
+    // measured 313 against 324 us per 16 such calls with the scattered
+    // flush, 210 against 208 us per 524288-token call).
+    const int64_t rounds = (n_tiles + wstride - 1) / wstride;
+    if (rounds >= 4 && nw * kWarpBytes >= kE * (kWin + 1) * 4) {
       // Coalesced: the window is first transposed into the (now idle) tile
       // buffers as rows r = 32 i + L (expert expert_of(L, i)) of 33 words, so
       // that a warp then adds one expert's 32 slots -- two runs of 16

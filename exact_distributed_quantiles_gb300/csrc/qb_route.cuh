@@ -58,7 +58,7 @@ struct Args {
   int64_t N;
   int k;
   int32_t* hist;  // hi: [E,256]  lo: [E,256]  k3: unused
-  uint16_t* keys_out;  // hi: EQB keys [N,E] (optional)  k3: bin indices [N,E]
+  uint16_t* keys_out;  // hi: EQB keys [N,E] (optional)
   int32_t* topk_out;
   float* alpha_out;
   const int32_t* sel;   // lo mode

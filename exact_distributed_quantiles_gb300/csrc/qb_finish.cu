@@ -214,13 +214,13 @@ __global__ void __cluster_dims__(kFinCluster, 1, 1) __launch_bounds__(kFinThread
                         int reset) {
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
-  __shared__ float q_s[64];                   // this CTA's quantiles
-  __shared__ float q_all[64 * kFinCluster];   // every CTA's, pushed by their owners
+  __shared__ float q_s[kMaxE / kFinCluster];  // this CTA's quantiles
+  __shared__ float q_all[kMaxE];              // every CTA's, pushed by their owners
   __shared__ double mu_s;
   // this CTA is running: other CTAs may write into its shared memory once
   // the matching wait has passed
   cluster_arrive_relaxed();
-  const int per = E / kFinCluster;  // experts of this CTA (4 .. 64)
+  const int per = E / kFinCluster;  // experts of this CTA (4 .. 128)
   const int j0 = rank * per;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int jl = warp; jl < per; jl += kFinThreads / 32) {
@@ -287,10 +287,10 @@ __global__ void __cluster_dims__(kFinCluster, 1, 1) __launch_bounds__(kFinThread
   cluster_wait();
   // every CTA derives the same mean from all E quantiles
   if (warp == 0) {
-    uint32_t u[16];
+    uint32_t u[kMaxE / 32];
     int bad = 0, emin = kNoExp, emax = -kNoExp;
 #pragma unroll
-    for (int h = 0; h < 16; ++h) {
+    for (int h = 0; h < kMaxE / 32; ++h) {
       const int j = lane + 32 * h;
       u[h] = j < E ? __float_as_uint(q_all[j]) : 0u;
       const int ex = (int)((u[h] >> 23) & 0xFFu);
@@ -310,7 +310,7 @@ __global__ void __cluster_dims__(kFinCluster, 1, 1) __launch_bounds__(kFinThread
       const int base_e = max(emin, 1);
       long long S = 0;
 #pragma unroll
-      for (int h = 0; h < 16; ++h) {
+      for (int h = 0; h < kMaxE / 32; ++h) {
         if (u[h] & 0x7FFFFFFFu) {
           const int ex = (int)((u[h] >> 23) & 0xFFu);
           const long long m = (long long)(((u[h] >> 16) & 0x7Fu) | (ex ? 0x80u : 0u));
@@ -352,7 +352,7 @@ __global__ void __cluster_dims__(kFinCluster, 1, 1) __launch_bounds__(kFinThread
 __global__ void __launch_bounds__(512) rank_average_kernel(const uint16_t* __restrict__ qkeys,
                                                            int P, int E,
                                                            float* __restrict__ bias_out) {
-  __shared__ double avg_s[512];
+  __shared__ double avg_s[kMaxE];
   __shared__ double mu_s;
   for (int j = threadIdx.x; j < E; j += blockDim.x) {
     double s = 0.0;
@@ -469,7 +469,7 @@ int launch_zero_i32(int32_t* p, int64_t n, cudaStream_t stream) {
 
 int launch_finalize(int32_t* hist_hi, int32_t* hist_lo, const int32_t* sel, const int32_t* r_lo,
                     int E, float* bias_out, uint16_t* qkey_out, int reset, cudaStream_t stream) {
-  if (E % kFinCluster != 0 || E / kFinCluster > 64) return QB_EUNSUPPORTED;
+  if (E % kFinCluster != 0 || E > kMaxE) return QB_EUNSUPPORTED;
   int log2E = 0;
   while ((1 << log2E) < E) ++log2E;
   if ((1 << log2E) != E) log2E = -1;  // not a power of two: the mean divides

@@ -18,8 +18,9 @@ inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Expert counts the kernels take: multiples of 32 from 32 to 512.
-inline bool supported_E(int E) { return E >= 32 && E <= 512 && E % 32 == 0; }
+// Expert counts the kernels take: multiples of 32 from 32 to kMaxE.
+constexpr int kMaxE = 1024;
+inline bool supported_E(int E) { return E >= 32 && E <= kMaxE && E % 32 == 0; }
 
 inline int launch_status() {
   return cudaPeekAtLastError() == cudaSuccess ? QB_OK : (cudaGetLastError(), QB_ECUDA);

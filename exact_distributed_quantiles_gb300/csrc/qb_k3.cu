@@ -315,15 +315,15 @@ __global__ void __cluster_dims__(kFinCluster, 1, 1) __launch_bounds__(kFinThread
                        float* __restrict__ bounds, float* __restrict__ bias_out, int reset) {
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
-  __shared__ double q_s[64];          // this CTA's quantiles
-  __shared__ double q_all[64 * kFinCluster];  // every CTA's, pushed by their owners
+  __shared__ double q_s[kMaxE / kFinCluster];  // this CTA's quantiles
+  __shared__ double q_all[kMaxE];              // every CTA's, pushed by their owners
   __shared__ double part_s[kFinCluster];
   __shared__ float mn_s[32], mx_s[32];
   __shared__ double mu_s;
   // (1) this CTA is running: other CTAs may write into its shared memory
   // once the matching wait has passed
   cluster_arrive_relaxed();
-  const int per = E / kFinCluster;  // experts of this CTA (4 .. 64)
+  const int per = E / kFinCluster;  // experts of this CTA (4 .. 128)
   const int j0 = rank * per;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const float lo = bounds[0], hi = bounds[1];
@@ -372,7 +372,7 @@ __global__ void __cluster_dims__(kFinCluster, 1, 1) __launch_bounds__(kFinThread
   if (warp < kFinCluster) {
     const double* qc = q_all + warp * per;
     double v = lane < per ? qc[lane] : 0.0;
-    if (lane + 32 < per) v = __dadd_rn(v, qc[lane + 32]);
+    for (int i = lane + 32; i < per; i += 32) v = __dadd_rn(v, qc[i]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = __dadd_rn(v, __shfl_down_sync(0xffffffffu, v, o));
     if (lane == 0) part_s[warp] = v;
@@ -440,7 +440,7 @@ int launch_k3_count(const void* logits, int dtype, const float* alpha, int64_t N
 
 int launch_k3_finalize(int32_t* hist, int E, int nbins, int64_t r, float* bounds, float* bias_out,
                        int reset, cudaStream_t stream) {
-  if (E % kFinCluster != 0 || E / kFinCluster > 64) return QB_EUNSUPPORTED;
+  if (E % kFinCluster != 0 || E > kMaxE) return QB_EUNSUPPORTED;
   k3_finalize_kernel<<<kFinCluster, kFinThreads, 0, stream>>>(hist, E, nbins, 1.0 / (double)nbins,
                                                               (long long)r, bounds, bias_out, reset);
   return launch_status();

@@ -101,9 +101,9 @@ __global__ void __cluster_dims__(kRhoCluster, 1, 1) __launch_bounds__(kRhoThread
                    int64_t batch_tokens, float* __restrict__ ws) {
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ int32_t sub[];  // [kRhoWarps][E]
-  __shared__ int32_t cnt[512];
+  __shared__ int32_t cnt[kMaxE];
   __shared__ float red[kRhoWarps];
-  __shared__ float t_s[512];
+  __shared__ float t_s[kMaxE];
   const int warp = threadIdx.x >> 5;
   const int rank = (int)cluster.block_rank();
   const int64_t b = blockIdx.x / kRhoCluster;
@@ -145,7 +145,7 @@ __global__ void __cluster_dims__(kRhoCluster, 1, 1) __launch_bounds__(kRhoThread
                       int64_t batch_tokens, int32_t* __restrict__ loads) {
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ int32_t sub[];  // [kRhoWarps][E]
-  __shared__ int32_t cnt[512];
+  __shared__ int32_t cnt[kMaxE];
   const int rank = (int)cluster.block_rank();
   const int64_t b = blockIdx.x / kRhoCluster;
   int64_t i0, i1;
@@ -331,10 +331,24 @@ __global__ void __maxnreg__(32) lei_apply_bulk_kernel(float* __restrict__ grad, 
 
 }  // namespace
 
+// The per-warp count rows take kRhoWarps * E int32 of dynamic shared memory,
+// 64 KB at E = 1024: above the default 48 KB, so the kernels opt in once.
+template <typename K>
+bool rho_smem_attr(K kern, bool& done) {
+  if (done) return true;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kRhoWarps * kMaxE * (int)sizeof(int32_t)) != cudaSuccess)
+    return false;
+  done = true;
+  return true;
+}
+
 int launch_maxvio(const int32_t* topk, int64_t N, int E, int k, int64_t batch_tokens,
                   int32_t* loads, double* out, cudaStream_t stream) {
   const int64_t nb = (N + batch_tokens - 1) / batch_tokens;
   const int smem = kRhoWarps * E * (int)sizeof(int32_t);
+  static bool attr = false;  // benign race (idempotent)
+  if (!rho_smem_attr(load_count_kernel, attr)) return launch_status();
   load_count_kernel<<<(unsigned)(nb * kRhoCluster), kRhoThreads, smem, stream>>>(
       topk, N, E, k, batch_tokens, loads);
   int st = launch_status();
@@ -347,6 +361,8 @@ int launch_lei_rho(const int32_t* topk, int64_t N, int E, int k, float eta,
                    int64_t batch_tokens, float* workspace, cudaStream_t stream) {
   const int64_t nb = (N + batch_tokens - 1) / batch_tokens;
   const int smem = kRhoWarps * E * (int)sizeof(int32_t);
+  static bool attr = false;  // benign race (idempotent)
+  if (!rho_smem_attr(lei_rho_kernel, attr)) return launch_status();
   lei_rho_kernel<<<(unsigned)(nb * kRhoCluster), kRhoThreads, smem, stream>>>(
       topk, N, E, k, eta, batch_tokens, workspace);
   return launch_status();

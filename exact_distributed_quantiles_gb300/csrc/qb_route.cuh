@@ -82,14 +82,15 @@ struct Geo {
   static constexpr int NSLOT = kWin + 1;                            // + dummy slot
   static constexpr int CSTRIDE = NSLOT * E + (NCOPY > 1 ? LPR : 0);  // words per copy
   static constexpr int STEPS = TILE * E / 256;                      // 256-element steps per tile
-  static constexpr int BREG = E == 512 ? 16 : 8;                    // per-lane bias registers
+  static constexpr int NQ = E >= 512 ? E / 256 : 1;                 // 256-expert quarters of a row
+  static constexpr int BREG = 8 * NQ;                               // per-lane bias registers
   // Position of expert e inside one histogram slot row: for a fixed element
   // index the 32 lanes of a step land in 32 distinct banks.
   __host__ __device__ static constexpr int pi(int e) {
-    return E == 512 ? (e >> 8) * 256 + (e & 7) * 32 + ((e & 255) >> 3) : (e & 7) * LPR + (e >> 3);
+    return E >= 512 ? (e >> 8) * 256 + (e & 7) * 32 + ((e & 255) >> 3) : (e & 7) * LPR + (e >> 3);
   }
   __device__ static __forceinline__ int pi_inv(int p) {
-    if (E == 512) {
+    if (E >= 512) {
       const int h = p >> 8, q = p & 255;
       return h * 256 + (q & 31) * 8 + (q >> 5);
     }
@@ -101,10 +102,28 @@ __host__ __device__ constexpr int round16(int b) { return (b + 15) & ~15; }
 
 // Bit mask over the groups of 8 experts of a token (32 bits up to E = 256).
 template <int G>
-using GroupMask = typename std::conditional<(G <= 32), uint32_t, unsigned long long>::type;
+using GroupMask = typename std::conditional<
+    (G <= 32), uint32_t,
+    typename std::conditional<(G <= 64), unsigned long long, unsigned __int128>::type>::type;
 __device__ __forceinline__ int lowest_bit(uint32_t m) { return __ffs((int)m) - 1; }  // -1 if 0
 __device__ __forceinline__ int lowest_bit(unsigned long long m) {
   return __ffsll((long long)m) - 1;
+}
+__device__ __forceinline__ int lowest_bit(unsigned __int128 m) {
+  const unsigned long long lo = (unsigned long long)m, hi = (unsigned long long)(m >> 64);
+  return lo ? __ffsll((long long)lo) - 1 : (hi ? 63 + __ffsll((long long)hi) : -1);
+}
+// OR of the group mask of lane ^ o
+__device__ __forceinline__ uint32_t shfl_xor_mask(uint32_t m, int o) {
+  return __shfl_xor_sync(0xffffffffu, m, o);
+}
+__device__ __forceinline__ unsigned long long shfl_xor_mask(unsigned long long m, int o) {
+  return __shfl_xor_sync(0xffffffffu, m, o);
+}
+__device__ __forceinline__ unsigned __int128 shfl_xor_mask(unsigned __int128 m, int o) {
+  const unsigned long long lo = __shfl_xor_sync(0xffffffffu, (unsigned long long)m, o);
+  const unsigned long long hi = __shfl_xor_sync(0xffffffffu, (unsigned long long)(m >> 64), o);
+  return ((unsigned __int128)hi << 64) | lo;
 }
 
 template <int E, typename T, int MODE, int TILE>
@@ -371,7 +390,7 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
   __syncthreads();
 
   // Per-lane expert block of the element-wise phases and its constants.
-  const int e0l = (E == 512) ? 8 * lane : (8 * lane) % E;
+  const int e0l = (E >= 512) ? 8 * lane : (8 * lane) % E;
   float breg[GE::BREG];
   int32_t selreg[GE::BREG];
 #pragma unroll
@@ -457,12 +476,17 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
 #pragma unroll
           for (int i = 0; i < 8; ++i) s[u][i] = 0.0f;
         }
-        const bool hi = (E == 512) && (st & 1);
+        const int qtr = st % GE::NQ;  // which 256-expert quarter of the row
         float v[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const f2_t B = hi ? f2_pack(breg[(8 + 2 * i) % GE::BREG], breg[(9 + 2 * i) % GE::BREG])
-                            : f2_pack(breg[2 * i], breg[2 * i + 1]);
+          float b0 = breg[2 * i], b1 = breg[2 * i + 1];
+#pragma unroll
+          for (int qq = 1; qq < GE::NQ; ++qq) {
+            b0 = qtr == qq ? breg[8 * qq + 2 * i] : b0;
+            b1 = qtr == qq ? breg[8 * qq + 2 * i + 1] : b1;
+          }
+          const f2_t B = f2_pack(b0, b1);
           f2_unpack(f2_add(f2_pack(s[u][2 * i], s[u][2 * i + 1]), B), v[2 * i], v[2 * i + 1]);
         }
         const float g = fmaxf(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])),
@@ -527,7 +551,7 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
       for (int g = 0; g < GH; ++g) cand |= (MaskT)(gm[g] >= tau ? 1u : 0u) << (h * GH + g);
       cand = actB ? cand : (MaskT)0;
 #pragma unroll
-      for (int o = TILE; o < 32; o <<= 1) cand |= __shfl_xor_sync(0xffffffffu, cand, o);
+      for (int o = TILE; o < 32; o <<= 1) cand |= shfl_xor_mask(cand, o);
 #pragma unroll
       for (int i = 0; i < KL; ++i) L[i] = -INFINITY;
       const float* srow = sc + t * E;
@@ -642,7 +666,7 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
           for (int g = 0; g < GH; ++g) gsel |= (MaskT)(gm[g] > alpha ? 1u : 0u) << (h * GH + g);
           gsel = actB ? gsel : (MaskT)0;
 #pragma unroll
-          for (int o = TILE; o < 32; o <<= 1) gsel |= __shfl_xor_sync(0xffffffffu, gsel, o);
+          for (int o = TILE; o < 32; o <<= 1) gsel |= shfl_xor_mask(gsel, o);
           const uint32_t below = (1u << (TILE * h)) - 1u;  // bits of the token's lower lanes
           const float* sp = srow + EPL * h;
           const float* bp = bias_s + EPL * h;
@@ -714,7 +738,7 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
             *reinterpret_cast<uint4*>(a.keys_out + tok * er + e0) =
                 make_uint4(kw[0], kw[1], kw[2], kw[3]);
           if constexpr (MODE == kModeHi) {
-            const uint32_t hoff = (E == 512 && (st & 1)) ? 1024u : 0u;  // +256 experts
+            const uint32_t hoff = 1024u * (uint32_t)(st % GE::NQ);  // +256 experts per quarter
             uint32_t mslot = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -728,7 +752,9 @@ __global__ void __launch_bounds__(Smem<E, T, MODE, TILE>::NW * 32, 1) route_kern
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const uint32_t key = (kw[i >> 1] >> ((i & 1) * 16)) & 0xFFFFu;
-              const int sl = (E == 512 && (st & 1)) ? selreg[(8 + i) % GE::BREG] : selreg[i];
+              int sl = selreg[i];
+#pragma unroll
+              for (int qq = 1; qq < GE::NQ; ++qq) sl = (st % GE::NQ) == qq ? selreg[8 * qq + i] : sl;
               if ((int)(key >> 8) == sl)
                 atomicAdd(a.hist + (int64_t)(e0 + i) * 256 + (key & 0xFFu), 1);
             }
@@ -804,6 +830,7 @@ int dispatch_E(int E, int k, const Args& a, cudaStream_t st) {
     QB_CASE(128)
     QB_CASE(256)
     QB_CASE(512)
+    QB_CASE(1024)
     default:
       return QB_EUNSUPPORTED;
   }

@@ -33,7 +33,7 @@
  *     of a global batch (qb_zero_i32), or let the finalize call reset them in
  *     place.  Counts are int32: the pooled token count must stay below 2^31.
  *   - Inputs must be finite; results on NaN logits are unspecified.
- *   - Supported expert counts: any multiple of 32 from 32 to 512 (rows of
+ *   - Supported expert counts: any multiple of 32 from 32 to 1024 (rows of
  *     a count that is not a power of two are processed in the tile of the
  *     next power of two, the extra experts masked).  The router GEMM takes
  *     E = 256 only.  Supported k: 1 <= k <= 15 and k < E.

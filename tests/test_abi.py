@@ -72,7 +72,7 @@ def test_argument_errors_are_reported_before_launch(lib):
     assert L.qb_route_hist_hi(fake, 0, fake, -1, 256, 6, fake, N0, N0, N0, N0) == lib.QB_EINVAL
     assert L.qb_route_hist_hi(fake, 0, fake, 1 << 31, 256, 6, fake, N0, N0, N0, N0) == lib.QB_EOVERFLOW
     # unsupported E, bad k
-    for E in (0, 16, 48, 544, 1024):
+    for E in (0, 16, 48, 1056, 2048):
         assert L.qb_route_hist_hi(fake, 0, fake, 10, E, 6, fake, N0, N0, N0, N0) == lib.QB_EUNSUPPORTED
     assert L.qb_route_hist_hi(fake, 0, fake, 10, 256, 0, fake, N0, N0, N0, N0) == lib.QB_EINVAL
     assert L.qb_route_hist_hi(fake, 0, fake, 10, 32, 32, fake, N0, N0, N0, N0) == lib.QB_EINVAL

@@ -36,7 +36,7 @@ def _logits(N, E, seed, dtype=torch.float32, std=1.0, off_std=0.5):
 
 
 # powers of two, and multiples of 32 that run padded to the next one
-ALL_E = [32, 64, 96, 128, 160, 256, 384, 480, 512]
+ALL_E = [32, 64, 96, 128, 160, 256, 384, 480, 512, 640, 1024]
 
 
 @pytest.mark.parametrize("E", ALL_E)
@@ -51,7 +51,7 @@ def test_route_small_shapes_fp32(qb, orc, E, k):
     assert np.array_equal(res["hist_hi"], orc.hist_hi(orc.keys(ref["margins"])))
 
 
-@pytest.mark.parametrize("E,k", [(64, 6), (96, 6), (256, 8), (384, 8), (512, 6)])
+@pytest.mark.parametrize("E,k", [(64, 6), (96, 6), (256, 8), (384, 8), (512, 6), (1024, 6)])
 @pytest.mark.parametrize("N", [1, 31, 32, 33, 1000])
 def test_route_bf16_and_ragged(qb, orc, E, k, N):
     x, b = _logits(N, E, seed=N + E, dtype=torch.bfloat16, std=1.5, off_std=0.3)
@@ -210,7 +210,7 @@ def test_full_step_layer_at_bench_size(qb, orc, layer):
 
 
 @pytest.mark.parametrize("E,k", [(32, 1), (64, 6), (96, 6), (128, 8), (160, 15), (256, 6),
-                                 (384, 8), (480, 6), (512, 15)])
+                                 (384, 8), (480, 6), (512, 15), (640, 6), (1024, 8)])
 def test_eqb_all_expert_counts(qb, orc, E, k):
     # the whole EQB chain (hi pass, select, lo pass from keys, finalize) for
     # every supported expert count, several tiles and a ragged tail

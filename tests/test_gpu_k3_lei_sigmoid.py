@@ -115,6 +115,7 @@ def test_k3_workload(qb, orc):
                                               (64, 6, 8000, torch.float32),   # global counts
                                               (96, 6, 1000, torch.bfloat16),  # padded rows
                                               (384, 8, 1000, torch.float32),
+                                              (1024, 8, 1000, torch.bfloat16),
                                               (32, 2, 1, torch.float32)])
 def test_k3_small_shapes(qb, orc, E, k, nbins, dtype):
     w = inputs.scaled(inputs.WORKLOADS["k3"], E=E, k=k, n_micro=3, n_tokens=32 * 5 + 3,
@@ -202,7 +203,7 @@ def test_lei_shapes_and_ragged_batches(qb, orc, N, E, k, bt):
 
 @pytest.mark.parametrize("N,E,k,bt", [(1, 32, 1, 0), (1000, 64, 6, 333), (4097, 512, 15, 1024),
                                       (70001, 256, 6, 4099), (5003, 160, 6, 777),
-                                      (4099, 480, 15, 1000)])
+                                      (4099, 480, 15, 1000), (2049, 1024, 8, 512)])
 def test_lei_rho_then_apply_equals_inject(qb, orc, N, E, k, bt):
     # The two halves on one stream give lei_inject's result bit for bit;
     # lei_apply alone is grad + workspace[batch(row)] in binary32 for every
@@ -239,7 +240,7 @@ def test_lei_rho_then_apply_equals_inject(qb, orc, N, E, k, bt):
 
 
 @pytest.mark.parametrize("N,E,bt", [(1, 32, 0), (1000, 64, 333), (4097, 512, 1024),
-                                    (3001, 96, 1000), (2049, 384, 512),
+                                    (3001, 96, 1000), (2049, 384, 512), (1031, 1024, 300),
                                     (70001, 256, 4099), (524288, 256, 32768)])
 def test_lei_apply_overlap_equals_apply(qb, N, E, bt):
     # The bulk-copy variant gives lei_apply's result bit for bit, alone and

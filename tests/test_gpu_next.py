@@ -64,7 +64,8 @@ def test_rank_average_pooled_workload(qb, orc, shards):
 
 
 @pytest.mark.parametrize("N,E,k,bt", [(131072, 256, 6, 32768), (1000, 64, 6, 333),
-                                      (4097, 512, 15, 1024), (77, 32, 1, 0)])
+                                      (4097, 512, 15, 1024), (77, 32, 1, 0),
+                                      (3001, 1024, 8, 1000), (2000, 352, 6, 640)])
 def test_maxvio(qb, orc, N, E, k, bt):
     topk = inputs.random_topk(N, E, k, seed=N + E, device="cuda")
     topk[: N // 5] = torch.arange(k, dtype=torch.int32, device="cuda")  # a hot set of experts

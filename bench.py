@@ -42,8 +42,8 @@ METRIC = "QB routed tokens/s per layer (E=256,k=6, 2-pass EQB) on 1 GB300; % of 
 # launch (route256_kernel, keys written, no top-k output) on a 524288-token
 # layer, from an ncu capture of that launch.  Reported only while the
 # kernel's sources hash to the value they had when the counters were taken.
-ROUTE_TRAFFIC = {"sha1": "4e94419a0530816f6ad800a3f78aa4d6ba16eca1", "tokens": 524288,
-                 "bytes": (537.009152 + 233.401600) * 1e6}
+ROUTE_TRAFFIC = {"sha1": "6d3af64790be3d0500bc64d8ab733e782b0e7a19", "tokens": 524288,
+                 "bytes": (537.001984 + 233.385728) * 1e6}
 ROUTE_SOURCES = ("qb_route256.cuh", "qb_route256_f32.cu", "qb_route.cuh", "qb_device.cuh")
 # Warp instructions of the same capture (smsp__inst_executed.sum), for the
 # issue-rate roofline of this issue-bound kernel; same hash guard.
@@ -52,7 +52,7 @@ ROUTE_INSTR = {"tokens": 524288, "warp_instructions": 127551415}
 # bf16 tokens: the alpha pass (route256_kernel, K3 mode) plus the count
 # kernel, from an ncu capture of those launches; reported while the K3
 # sources hash to the value they had when it was taken.
-K3_INSTR = {"sha1": "7784671ffd5e7498d4df8c2e54365695b2852ea5", "tokens": 65536,
+K3_INSTR = {"sha1": "0149e05d688fd7c72b462d21df2635206c46e089", "tokens": 65536,
             "warp_instructions": 13063568 + 13192792}
 K3_SOURCES = ("qb_route256.cuh", "qb_route256_bf16.cu", "qb_route.cuh", "qb_device.cuh",
               "qb_k3.cu")

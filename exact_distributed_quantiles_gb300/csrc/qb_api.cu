@@ -259,7 +259,7 @@ int qb_router_gemm(const void* hidden, const void* w_t, int64_t M, int H, int E,
   if (!aligned16(hidden) || !aligned16(w_t) || !aligned16(logits_out)) return QB_EINVAL;
   if (M < 0) return QB_EINVAL;
   if (M > INT32_MAX) return QB_EOVERFLOW;
-  if (E != 256 || H < 64 || H % 64 != 0) return QB_EUNSUPPORTED;
+  if (E < 32 || E > 256 || E % 32 != 0 || H < 64 || H % 64 != 0) return QB_EUNSUPPORTED;
   if (M == 0) return QB_OK;
   return launch_router_gemm(hidden, w_t, M, H, E, logits_out, as_stream(stream));
 }

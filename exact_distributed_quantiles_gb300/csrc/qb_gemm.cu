@@ -5,12 +5,13 @@
 // scores from hidden states; the histogram passes then run on those scores
 // ("Implementation": the fused path extends the existing router kernel).
 //
-// One persistent CTA per SM walks tiles of 128 x 256 logits (all experts of
-// 128 tokens), tile = blockIdx.x + i * gridDim.x:
-//   warp 0      TMA producer: hidden tile 128 x 64 and W^T tile 256 x 64 per
+// One persistent CTA per SM walks tiles of 128 x E logits (all experts of
+// 128 tokens; E a multiple of 32 up to 256), tile = blockIdx.x + i * gridDim.x:
+//   warp 0      TMA producer: hidden tile 128 x 64 and W^T tile E x 64 per
 //               stage (bf16, 128-byte swizzle) into a 4-deep ring;
-//   warp 1      allocates 512 TMEM columns (two accumulators); one lane issues
-//               tcgen05.mma (M=128, N=256, K=16) four times per stage into
+//   warp 1      allocates 512 TMEM columns (two accumulators of up to 256
+//               columns); one lane issues tcgen05.mma (M=128, N=E, K=16)
+//               four times per stage into
 //               accumulator (local tile index & 1), commits each stage back to
 //               the producer and each finished tile to its epilogue;
 //   warps 2-9   two epilogue warpgroups, warpgroup b draining accumulator b
@@ -34,7 +35,7 @@ namespace qb {
 namespace {
 
 constexpr int kBM = 128;        // tokens per tile (TMEM lanes)
-constexpr int kBN = 256;        // experts per tile (TMEM columns per accumulator)
+constexpr int kBN = 256;        // TMEM columns per accumulator (the largest expert count)
 constexpr int kBK = 64;         // K per stage: one 128-byte swizzle row of bf16
 constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK * 2;  // 16 KB
@@ -44,13 +45,14 @@ constexpr int kEpiWarps = 8;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
 
-constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN);
 
 struct GemmArgs {
-  float* logits;  // [M, 256] fp32
+  float* logits;  // [M, E] fp32
   int64_t M;
   int K;
   int* status;
+  int E;  // experts: the MMA's N (a multiple of 32, at most 256)
+  uint32_t idesc;  // instruction descriptor for M = 128, N = E
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -103,7 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t sa = base + (uint32_t)(s * kStageBytes);
-          mbar_arrive_expect_tx(full + s, (uint32_t)kStageBytes);
+          mbar_arrive_expect_tx(full + s, (uint32_t)(kABytes + g.E * kBK * 2));
           tma_load_2d(sa, &map_a, kt * kBK, (int)(tile * kBM), smem_u32(full + s));
           tma_load_2d(sa + kABytes, &map_b, kt * kBK, 0, smem_u32(full + s));
         }
@@ -111,6 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
+      const uint32_t idesc = g.idesc;
       uint32_t gk = 0, lt = 0;
       bool ok = true;
       for (int64_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++lt) {
@@ -131,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the 16-element K slice starts 32 bytes further along the row
             const uint64_t ad = smem_desc_sw128(sa + 32u * kk);
             const uint64_t bd = smem_desc_sw128(sa + kABytes + 32u * kk);
-            tc_mma(d, ad, bd, kIdesc, (kt > 0 || kk > 0) ? 1u : 0u);
+            tc_mma(d, ad, bd, idesc, (kt > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(smem_u32(empty + s));  // frees the stage once these MMAs are done
         }
@@ -153,11 +156,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t row = tile * kBM + 32 * q + lane;
       const uint32_t lane_base = tmem + (uint32_t)(wg * kBN) + ((uint32_t)(32 * q) << 16);
 #pragma unroll 1
-      for (int c0 = 0; c0 < kBN; c0 += 32) {
+      for (int c0 = 0; c0 < g.E; c0 += 32) {
         uint32_t r[32];
         tmem_ld32(lane_base + (uint32_t)c0, r);
         if (row < g.M) {
-          float4* dst = reinterpret_cast<float4*>(g.logits + row * kBN + c0);
+          float4* dst = reinterpret_cast<float4*>(g.logits + row * g.E + c0);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
@@ -213,13 +216,13 @@ bool make_bf16_kmajor_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint
 
 int launch_router_gemm(const void* hidden, const void* w_t, int64_t M, int K, int E,
                        float* logits, cudaStream_t stream) {
-  if (E != kBN) return QB_EUNSUPPORTED;
+  if (E < 32 || E > kBN || E % 32 != 0) return QB_EUNSUPPORTED;
   if (K % kBK != 0 || K <= 0) return QB_EUNSUPPORTED;
   if (!encode_fn()) return QB_ECUDA;
   CUtensorMap ma, mb;
   if (!make_map(&ma, hidden, (uint64_t)M, (uint64_t)K, kBM)) return QB_EINVAL;
-  if (!make_map(&mb, w_t, (uint64_t)E, (uint64_t)K, kBN)) return QB_EINVAL;
-  GemmArgs g{logits, M, K, device_status_ptr()};
+  if (!make_map(&mb, w_t, (uint64_t)E, (uint64_t)K, (uint32_t)E)) return QB_EINVAL;
+  GemmArgs g{logits, M, K, device_status_ptr(), E, idesc_bf16_f32(kBM, E)};
   if (!g.status) return QB_ECUDA;
   static bool attr = false;
   if (!attr) {

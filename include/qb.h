@@ -242,7 +242,8 @@ int lei_apply_overlap(float* grad, int64_t N, int E, int64_t batch_tokens, const
  *   w_t        device bf16 [E, H]: W transposed (each expert's column of W
  *              contiguous), 16-byte aligned.
  *   logits_out device fp32 [M, E], 16-byte aligned.
- * Supported: E = 256, H a positive multiple of 64.  The accumulation order
+ * Supported: E a multiple of 32 from 32 to 256 (the MMA's N), H a positive
+ * multiple of 64.  The accumulation order
  * over H is the tensor core's; results agree with an fp64 product within
  * fp32 accumulation error. */
 int qb_router_gemm(const void* hidden, const void* w_t, int64_t M, int H, int E, float* logits_out,

@@ -36,14 +36,16 @@ def _check_gemm(logits, hidden, W):
     return exact
 
 
-@pytest.mark.parametrize("M,H", [(128, 64), (300, 128), (1000, 2048), (129, 1024)])
-def test_router_gemm_small(qb, M, H):
+@pytest.mark.parametrize("M,H,E", [(128, 64, 256), (300, 128, 256), (1000, 2048, 256),
+                                   (129, 1024, 256), (1000, 512, 32), (333, 256, 96),
+                                   (700, 2048, 160), (257, 128, 224)])
+def test_router_gemm_small(qb, M, H, E):
     g = torch.Generator(device="cuda")
-    g.manual_seed(M + H)
+    g.manual_seed(M + H + E)
     hidden = torch.randn(M, H, generator=g, device="cuda").to(torch.bfloat16)
-    W = (torch.randn(H, 256, generator=g, device="cuda") * H ** -0.5).to(torch.bfloat16)
+    W = (torch.randn(H, E, generator=g, device="cuda") * H ** -0.5).to(torch.bfloat16)
     w_t = W.t().contiguous()
-    logits = torch.full((M, 256), float("nan"), dtype=torch.float32, device="cuda")
+    logits = torch.full((M, E), float("nan"), dtype=torch.float32, device="cuda")
     qb.qb_router_gemm(hidden, w_t, logits)
     torch.cuda.synchronize()
     assert qb.device_status() == 0

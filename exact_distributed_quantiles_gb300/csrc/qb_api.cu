@@ -274,12 +274,22 @@ int qb_router_gemm_hist_hi(const void* hidden, const void* w_t, int64_t M, int H
     return QB_EINVAL;
   if (M < 0) return QB_EINVAL;
   if (M > INT32_MAX) return QB_EOVERFLOW;
-  if (E != 256 || H < 64 || H % 64 != 0) return QB_EUNSUPPORTED;
+  if (E < 32 || E > 256 || E % 32 != 0 || H < 64 || H % 64 != 0) return QB_EUNSUPPORTED;
   if (k < 1 || k >= E) return QB_EINVAL;
   if (k > 15) return QB_EUNSUPPORTED;
+  if (E != 256 && !logits_out) return QB_EUNSUPPORTED;
   if (M == 0) return QB_OK;
-  return launch_router_gemm_route(hidden, w_t, M, H, k, bias, hist_hi, keys_out, topk_out,
-                                  alpha_out, logits_out, as_stream(stream));
+  if (E == 256)
+    return launch_router_gemm_route(hidden, w_t, M, H, k, bias, hist_hi, keys_out, topk_out,
+                                    alpha_out, logits_out, as_stream(stream));
+  // Other expert counts: the plain GEMM into logits_out, then the routing
+  // pass on those logits (two launches; the fused epilogue is built for 256
+  // experts).  The results are the same: the fused kernel equals the routing
+  // pass run on its own logits.
+  int st = launch_router_gemm(hidden, w_t, M, H, E, logits_out, as_stream(stream));
+  if (st != QB_OK) return st;
+  return launch_route_hi(logits_out, QB_F32, bias, M, E, k, hist_hi, keys_out, topk_out,
+                         alpha_out, nullptr, nullptr, 0, as_stream(stream));
 }
 
 int qb_rank_average(const uint16_t* qkeys, int P, int E, float* bias_out, void* stream) {

@@ -257,9 +257,11 @@ int qb_router_gemm(const void* hidden, const void* w_t, int64_t M, int H, int E,
  * binary32 steps): hist_hi += counts; keys_out, topk_out, alpha_out as in
  * qb_route_hist_hi (each optional); logits_out optional (fp32 [M, E],
  * written only when given, e.g. to check the outputs).  Arguments as in
- * qb_router_gemm and qb_route_hist_hi; E = 256, 1 <= k <= 15.  One launch:
+ * qb_router_gemm and qb_route_hist_hi; 1 <= k <= 15.  E = 256: one launch,
  * a persistent CTA per SM; tokens with more than 8 candidate groups of 8
- * experts (ties) or a tie at alpha take a slower exact path. */
+ * experts (ties) or a tie at alpha take a slower exact path.  Other E (a
+ * multiple of 32 up to 256) require logits_out (QB_EUNSUPPORTED without
+ * it): qb_router_gemm into logits_out, then qb_route_hist_hi on it. */
 int qb_router_gemm_hist_hi(const void* hidden, const void* w_t, int64_t M, int H, int E, int k,
                            const float* bias, float* logits_out, int32_t* hist_hi,
                            uint16_t* keys_out, int32_t* topk_out, float* alpha_out,

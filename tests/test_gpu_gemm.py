@@ -116,6 +116,35 @@ def test_fused_epilogue_matches_routing_of_its_logits(qb, orc, M, H, k):
         assert np.array_equal(res2[key], res[key]), key
 
 
+@pytest.mark.parametrize("M,H,E,k", [(700, 256, 96, 6), (300, 512, 160, 8), (129, 64, 32, 1)])
+def test_fused_entry_other_expert_counts(qb, orc, M, H, E, k):
+    # E != 256: the GEMM into logits_out, then the routing pass on it; the
+    # same outputs as the routing pass on those logits, and no logits_out
+    # is refused
+    g = torch.Generator(device="cuda")
+    g.manual_seed(M + H + E + k)
+    hidden = torch.randn(M, H, generator=g, device="cuda").to(torch.bfloat16)
+    W = (torch.randn(H, E, generator=g, device="cuda") * H ** -0.5).to(torch.bfloat16)
+    w_t = W.t().contiguous()
+    bias = (torch.rand(E, generator=g, device="cuda") * 2 - 1) * 0.1
+    logits = torch.empty(M, E, dtype=torch.float32, device="cuda")
+    hist = torch.zeros(E, 256, dtype=torch.int32, device="cuda")
+    keys = torch.empty(M, E, dtype=torch.int16, device="cuda")
+    topk = torch.empty(M, k, dtype=torch.int32, device="cuda")
+    alpha = torch.empty(M, dtype=torch.float32, device="cuda")
+    qb.qb_router_gemm_hist_hi(hidden, w_t, bias, k, logits, hist, keys_out=keys, topk_out=topk,
+                              alpha_out=alpha)
+    torch.cuda.synchronize()
+    assert qb.device_status() == 0
+    _check_gemm(logits, hidden, W)
+    res = dict(hist=hist.cpu().numpy(), keys=keys.cpu().numpy().view(np.uint16),
+               topk=topk.cpu().numpy(), alpha=alpha.cpu().numpy())
+    ref = assert_route_matches(orc, res, logits.cpu().numpy(), bias.cpu().numpy(), k)
+    assert np.array_equal(res["hist"], orc.hist_hi(orc.keys(ref["margins"])))
+    with pytest.raises(qb.QBError):
+        qb.qb_router_gemm_hist_hi(hidden, w_t, bias, k, None, hist)
+
+
 def test_fused_epilogue_exact_path_on_ties(qb, orc):
     # W's 256 columns repeat 8 distinct ones: every group of 8 experts holds
     # the same values, so all 32 groups tie at tau (more candidates than the

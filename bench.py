@@ -42,8 +42,8 @@ METRIC = "QB routed tokens/s per layer (E=256,k=6, 2-pass EQB) on 1 GB300; % of 
 # launch (route256_kernel, keys written, no top-k output) on a 524288-token
 # layer, from an ncu capture of that launch.  Reported only while the
 # kernel's sources hash to the value they had when the counters were taken.
-ROUTE_TRAFFIC = {"sha1": "6d3af64790be3d0500bc64d8ab733e782b0e7a19", "tokens": 524288,
-                 "bytes": (537.001984 + 233.385728) * 1e6}
+ROUTE_TRAFFIC = {"sha1": "733d5b135ec5fdf43ac877848a87446b3b31cb27", "tokens": 524288,
+                 "bytes": (537.002496 + 233.244416) * 1e6}
 ROUTE_SOURCES = ("qb_route256.cuh", "qb_route256_f32.cu", "qb_route.cuh", "qb_device.cuh")
 # Warp instructions of the same capture (smsp__inst_executed.sum), for the
 # issue-rate roofline of this issue-bound kernel; same hash guard.
@@ -52,8 +52,8 @@ ROUTE_INSTR = {"tokens": 524288, "warp_instructions": 127551415}
 # bf16 tokens: the alpha pass (route256_kernel, K3 mode) plus the count
 # kernel, from an ncu capture of those launches; reported while the K3
 # sources hash to the value they had when it was taken.
-K3_INSTR = {"sha1": "0149e05d688fd7c72b462d21df2635206c46e089", "tokens": 65536,
-            "warp_instructions": 13063568 + 13192792}
+K3_INSTR = {"sha1": "dccb81e1ccf1808612a8277b94163e0f3bb02a94", "tokens": 65536,
+            "warp_instructions": 12817808 + 13192792}
 K3_SOURCES = ("qb_route256.cuh", "qb_route256_bf16.cu", "qb_route.cuh", "qb_device.cuh",
               "qb_k3.cu")
 UNIT = "tokens/s/layer"

@@ -164,6 +164,42 @@ __device__ __forceinline__ float select_with_partner(const float (&L)[KL], const
   return best;
 }
 
+// Lists of KL = 16 entries whose last 8 are -inf (a block of 8 sorted into
+// an empty list): the general merges would take element-wise maxima against
+// -inf; these give the same lists with half the shuffles and no maxima.
+// Lane ^ o's 8 values, reversed after this lane's 8, form a bitonic sequence
+// that the bitonic merger sorts.
+__device__ __forceinline__ void bitonic_clean16(float (&L)[16]) {
+#pragma unroll
+  for (int d = 8; d >= 1; d /= 2) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if ((i & d) == 0) route::cas_desc(L[i], L[i + d]);
+  }
+}
+__device__ __forceinline__ void merge_partner_8of16(float (&L)[16], int o) {
+  float P[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) P[i] = __shfl_xor_sync(0xffffffffu, L[i], o);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) L[8 + j] = P[7 - j];
+  bitonic_clean16(L);
+}
+// a block of 8 values into such a list
+__device__ __forceinline__ void append_block8_16(float (&L)[16], float (&v)[8]) {
+  route::sort8_desc(v);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) L[8 + j] = v[7 - j];
+  bitonic_clean16(L);
+}
+template <int KL>
+__device__ __forceinline__ void merge_partner_first(float (&L)[KL], int o) {
+  if constexpr (KL == 16)
+    merge_partner_8of16(L, o);
+  else
+    route::merge_partner<KL>(L, o);
+}
+
 template <int KL, int M>
 __device__ __forceinline__ void partner_head(const float (&L)[KL], float (&P)[KL], int o) {
 #pragma unroll
@@ -397,7 +433,7 @@ __device__ __forceinline__ bool tile_pass(const Ctx& c, const float (&breg)[8], 
       for (int i = 0; i < 8; ++i) w8[i] = gm[i];
       route::first_block8<KL>(L, w8);
     }
-    route::merge_partner<KL>(L, 8);
+    merge_partner_first<KL>(L, 8);
     float tau;
     if constexpr (K1 > 0) {
       float P[KL];
@@ -462,7 +498,14 @@ __device__ __forceinline__ bool tile_pass(const Ctx& c, const float (&breg)[8], 
           group_v(trow, c.bias_s, gr[r] < 0 ? 0 : gr[r], w8);
 #pragma unroll
           for (int i = 0; i < 8; ++i) w8[i] = gr[r] < 0 ? -INFINITY : w8[i];
-          route::merge_block8<KL>(L, w8);
+          if constexpr (KL == 16) {
+            if (r == 1)
+              append_block8_16(L, w8);  // round 0 left 8 values and 8 -inf
+            else
+              route::merge_block8<KL>(L, w8);
+          } else {
+            route::merge_block8<KL>(L, w8);
+          }
         }
       }
     }

@@ -214,12 +214,13 @@ class FullStep:
         # the top-k sets are LEI's input only: EQB alone does not produce them
         if per_microbatch:
             # one hi-pass call per 32768-token microbatch, as they would arrive
+            # (each after the first continues the batch: qb_route_hist_hi_next)
             n = w.n_tokens
             for m in range(w.n_micro):
                 sl = slice(m * n, (m + 1) * n)
-                qb.qb_route_hist_hi(lg[sl], self.bias[l], w.k, self.hist_hi[l],
-                                    keys_out=self.keys[sl],
-                                    topk_out=self.topk[j][sl] if lei else None)
+                route = qb.qb_route_hist_hi if m == 0 else qb.qb_route_hist_hi_next
+                route(lg[sl], self.bias[l], w.k, self.hist_hi[l], keys_out=self.keys[sl],
+                      topk_out=self.topk[j][sl] if lei else None)
         else:
             qb.qb_route_hist_hi(lg, self.bias[l], w.k, self.hist_hi[l], keys_out=self.keys,
                                 topk_out=self.topk[j] if lei else None)

@@ -130,6 +130,24 @@ int qb_route_hist_hi(const void* logits, int dtype, const float* bias, int64_t N
                          nullptr, nullptr, 0, as_stream(stream));
 }
 
+int qb_route_hist_hi_next(const void* logits, int dtype, const float* bias, int64_t N, int E,
+                          int k, int32_t* hist_hi, uint16_t* keys_out, int32_t* topk_out,
+                          float* alpha_out, void* stream) {
+  int st = check_route_args(logits, dtype, bias, N, E, k);
+  if (st != QB_OK) return st;
+  if (!hist_hi) return QB_EINVAL;
+  if (keys_out && !aligned16(keys_out)) return QB_EINVAL;
+  if (N == 0) return QB_OK;
+  if (E == 256 && dtype == QB_F32)
+    return launch_route256_hi_f32(logits, bias, N, k, hist_hi, keys_out, topk_out, alpha_out,
+                                  as_stream(stream), true);
+  if (E == 256)
+    return launch_route256_hi_bf16(logits, bias, N, k, hist_hi, keys_out, topk_out, alpha_out,
+                                   as_stream(stream), true);
+  return launch_route_hi(logits, dtype, bias, N, E, k, hist_hi, keys_out, topk_out, alpha_out,
+                         nullptr, nullptr, 0, as_stream(stream));
+}
+
 int qb_select_hi(const int32_t* hist_hi, int E, int64_t r, int32_t* sel, int32_t* r_lo,
                  void* stream) {
   if (!hist_hi || !sel || !r_lo) return QB_EINVAL;

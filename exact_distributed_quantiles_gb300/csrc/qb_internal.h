@@ -36,13 +36,15 @@ int launch_route_lo(const void* logits, int dtype, const float* bias, int64_t N,
 int launch_route_k3(const void* logits, int dtype, const float* bias, int64_t N, int E, int k,
                     int32_t* hist, uint16_t* keys_out, int32_t* topk_out, float* alpha_out,
                     const int32_t* sel, const float* bounds, int nbins, cudaStream_t stream);
-// EQB hi pass specialised to E = 256 (qb_route256.cuh), per input type.
+// EQB hi pass specialised to E = 256 (qb_route256.cuh), per input type;
+// chained: a further microbatch right after another such call on the stream
+// (qb_route_hist_hi_next).
 int launch_route256_hi_f32(const void* logits, const float* bias, int64_t N, int k,
                            int32_t* hist, uint16_t* keys_out, int32_t* topk_out,
-                           float* alpha_out, cudaStream_t stream);
+                           float* alpha_out, cudaStream_t stream, bool chained = false);
 int launch_route256_hi_bf16(const void* logits, const float* bias, int64_t N, int k,
                             int32_t* hist, uint16_t* keys_out, int32_t* topk_out,
-                            float* alpha_out, cudaStream_t stream);
+                            float* alpha_out, cudaStream_t stream, bool chained = false);
 // alpha per token only (the first half of the K3 pass), E = 256.
 int launch_route256_alpha_f32(const void* logits, const float* bias, int64_t N, int k,
                               float* alpha_out, cudaStream_t stream);

@@ -71,6 +71,10 @@ struct Args {
   // padded experts get bias -inf and score 0, so v = -inf keeps them out of
   // the top-(k+1), and nothing of theirs is stored or counted.
   int e_real;
+  // E = 256 pass only: the call continues a global batch right after another
+  // such call on the same stream (qb_route_hist_hi_next): it skips the wait
+  // for the previous kernel at its start and waits at its end instead.
+  int chained = 0;
 };
 
 template <int E, int TILE>

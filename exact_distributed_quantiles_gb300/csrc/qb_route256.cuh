@@ -45,6 +45,7 @@ constexpr int kPairs = kTile / 2;  // row pairs per tile, one mbarrier each
 constexpr int kWin = route::kWin;
 constexpr int kDummy = route::kDummy;
 constexpr int kHistBytes = (kWin + 1) * kE * 4;  // [slot][i * 32 + lane] int32
+constexpr int kStg = 36;  // words per staged window row at the flush (144 bytes)
 
 // Modes of the pass: the EQB hi pass (phases A-C), or alpha only (phases A
 // and B: alpha per token, the input of the K3 counting kernel).
@@ -687,9 +688,6 @@ __global__ void __launch_bounds__(warps_max(MODE) * 32, 1) route256_kernel(const
   __shared__ __align__(16) float bias_s[kE];
   const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
   const int lane = threadIdx.x & 31;
-  // a kernel launched as this one's programmatic dependent (lei_apply_overlap)
-  // may be scheduled into the room left beside this CTA from now on
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   int32_t* hist_s = reinterpret_cast<int32_t*>(smem);
   unsigned char* wb = smem + hist_bytes(MODE) + warp * kWarpBytes;
   Ctx c;
@@ -707,8 +705,17 @@ __global__ void __launch_bounds__(warps_max(MODE) * 32, 1) route256_kernel(const
     for (int i = threadIdx.x; i < (kWin + 1) * kE; i += blockDim.x) hist_s[i] = 0;
   // Launched as a programmatic dependent of the kernel before it: this CTA
   // may have started while that kernel still runs, so wait for its
-  // completion (and its memory) before the first global access.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // completion (and its memory) before the first global access.  A chained
+  // call follows another hi pass of the same global batch, which has itself
+  // waited before it let this one launch: nothing this call reads is still
+  // being written, and its counts only add to the same histogram, so it
+  // starts at once (and waits at its end, so that it completes after the
+  // call before it).
+  if (!a.chained) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // From here on, a kernel launched as this one's programmatic dependent (the
+  // next chained call, or lei_apply_overlap) may take the room this CTA
+  // leaves: everything before this kernel has completed.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int i = threadIdx.x; i < kE; i += blockDim.x) bias_s[i] = a.bias[i];
   if (lane == 0) {
     // one arrival per lane per phase: each lane's cp.async completions
@@ -745,39 +752,48 @@ __global__ void __launch_bounds__(warps_max(MODE) * 32, 1) route256_kernel(const
     parity ^= 1u;
   }
 
-  // ---- flush the shared window: one global atomic per non-zero counter
+  // ---- flush the shared window
   if constexpr (MODE == kHi256) {
     const int nw = (int)(blockDim.x >> 5);
-    // The transposed flush costs each CTA two more barriers and a pass over
-    // the window in shared memory; it pays when the launch is long (many
-    // rounds of tiles: the scattered adds of 152 CTAs then contend in L2),
-    // not for a launch of a few rounds (a 32768-token microbatch: 2 rounds;
-    // measured 313 against 324 us per 16 such calls with the scattered
-    // flush, 210 against 208 us per 524288-token call).
-    const int64_t rounds = (n_tiles + wstride - 1) / wstride;
-    if (rounds >= 4 && nw * kWarpBytes >= kE * (kWin + 1) * 4) {
-      // Coalesced: the window is first transposed into the (now idle) tile
-      // buffers as rows r = 32 i + L (expert expert_of(L, i)) of 33 words, so
-      // that a warp then adds one expert's 32 slots -- two runs of 16
-      // consecutive words of its histogram row (hi bytes 0xB0-0xBF and
-      // 0x40-0x4F) -- instead of 32 counters of 32 different experts.  Both
-      // copies are conflict-free: word (r, slot) sits in bank (r + slot) % 32.
+    if ((reinterpret_cast<uintptr_t>(a.hist) & 15) == 0 && nw * kWarpBytes >= kE * kStg * 4) {
+      // Through the (now idle) tile buffers: the window is copied into rows
+      // r = 32 i + L (expert expert_of(L, i)) of kStg words, whose slots 0-15
+      // and 16-31 are two runs of 16 consecutive counters of the expert's
+      // histogram row (hi bytes 0xB0-0xBF and 0x40-0x4F); each run is then
+      // added by one 64-byte bulk reduction in L2 (512 per CTA instead of
+      // one atomic per counter).  Both copies are conflict-free: the reads
+      // take 32 consecutive words, and the 16-byte writes of a quarter-warp
+      // land on 8 different 16-byte bank groups ((9 r + q) % 8 differs).
       // Every lane first waits for its own row copies (after a timed-out
-      // wait some may still be landing in those buffers).
+      // wait some may still be landing in those buffers) and the row-pair
+      // barriers living in the buffers are invalidated.
       asm volatile("cp.async.wait_all;" ::: "memory");
+      if (lane == 0)
+        for (int q = 0; q < kPairs; ++q)
+          asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(c.bars + q))
+                       : "memory");
       __syncthreads();
       int32_t* stg = reinterpret_cast<int32_t*>(smem + hist_bytes(MODE));
-      for (int p = warp; p < kWin * 8; p += nw) {
-        const int i = p & 7, slot = p >> 3;
-        stg[(32 * i + lane) * (kWin + 1) + slot] = hist_s[lane + 32 * i + 256 * slot];
+      for (int p = warp; p < 8 * (kWin / 4); p += nw) {
+        const int i = p & 7, q = p >> 3;  // rows 32 i + lane, slots 4q .. 4q+3
+        const int32_t* src = hist_s + lane + 32 * i + 256 * (4 * q);
+        *reinterpret_cast<int4*>(stg + (32 * i + lane) * kStg + 4 * q) =
+            make_int4(src[0], src[256], src[512], src[768]);
       }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncthreads();
-      for (int r = warp; r < kE; r += nw) {
-        const int cnt = stg[r * (kWin + 1) + lane];
-        if (cnt)
-          atomicAdd(a.hist + (int64_t)expert_of(r & 31, r >> 5) * 256 + slot_bin(lane), cnt);
+      for (int j = threadIdx.x; j < 2 * kE; j += blockDim.x) {
+        const int r = j >> 1, run = j & 1;
+        int32_t* dst = a.hist + (int64_t)expert_of(r & 31, r >> 5) * 256 + (run ? 0x40 : 0xB0);
+        asm volatile(
+            "cp.reduce.async.bulk.global.shared::cta.bulk_group.add.u32 [%0], [%1], 64;" ::"l"(dst),
+            "r"(smem_u32(stg + r * kStg + 16 * run))
+            : "memory");
       }
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     } else {
+      // a histogram that is not 16-byte aligned: one atomic per non-zero counter
       __syncthreads();
       for (int w = threadIdx.x; w < kWin * kE; w += blockDim.x) {
         const int cnt = hist_s[w];
@@ -788,6 +804,7 @@ __global__ void __launch_bounds__(warps_max(MODE) * 32, 1) route256_kernel(const
       }
     }
   }
+  if (a.chained) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <typename T, int KL, int K1, int MODE>
@@ -849,9 +866,11 @@ int dispatch_k(int k, const Args& a, cudaStream_t st) {
 // qb_route256_bf16.cu.
 template <typename T>
 int launch_hi_t(const void* logits, const float* bias, int64_t N, int k, int32_t* hist,
-                uint16_t* keys_out, int32_t* topk_out, float* alpha_out, cudaStream_t stream) {
+                uint16_t* keys_out, int32_t* topk_out, float* alpha_out, cudaStream_t stream,
+                bool chained = false) {
   Args a{logits, bias, N, k, hist, keys_out, topk_out, alpha_out, nullptr, nullptr, 0,
          device_status_ptr(), kE};
+  a.chained = chained ? 1 : 0;
   if (!a.status) return QB_ECUDA;
   return dispatch_k<T, kHi256>(k, a, stream);
 }

@@ -21,7 +21,8 @@ QB_F32, QB_BF16 = 0, 1
 
 EXPORTS = ("qb_status_string", "qb_version", "qb_rank", "qb_sigmoid", "qb_sigmoid_scalar",
            "qb_zero_i32",
-           "qb_route_hist_hi", "qb_select_hi", "qb_keys_hist_lo", "qb_route_hist_lo",
+           "qb_route_hist_hi", "qb_route_hist_hi_next", "qb_select_hi", "qb_keys_hist_lo",
+           "qb_route_hist_lo",
            "qb_finalize", "k3_route_hist", "k3_finalize", "lei_inject", "qb_device_status",
            "lei_inject_noalloc", "qb_router_gemm", "qb_router_gemm_hist_hi", "qb_rank_average",
            "qb_maxvio", "lei_rho", "lei_apply",
@@ -48,6 +49,7 @@ def _load():
         "qb_sigmoid_scalar": (I, [P, P, I64, P]),
         "qb_zero_i32": (I, [P, I64, P]),
         "qb_route_hist_hi": (I, [P, I, P, I64, I, I, P, P, P, P, P]),
+        "qb_route_hist_hi_next": (I, [P, I, P, I64, I, I, P, P, P, P, P]),
         "qb_select_hi": (I, [P, I, I64, P, P, P]),
         "qb_keys_hist_lo": (I, [P, I64, I, P, P, P]),
         "qb_route_hist_lo": (I, [P, I, P, I64, I, I, P, P, P]),
@@ -139,6 +141,15 @@ def qb_route_hist_hi(logits, bias, k, hist_hi, keys_out=None, topk_out=None, alp
            lib.qb_route_hist_hi(_ptr(logits), _dtype(logits), _ptr(bias), N, E, int(k),
                                 _ptr(hist_hi), _ptr(keys_out), _ptr(topk_out), _ptr(alpha_out),
                                 _stream(stream)))
+
+
+def qb_route_hist_hi_next(logits, bias, k, hist_hi, keys_out=None, topk_out=None,
+                          alpha_out=None, stream=None):
+    N, E = logits.shape
+    _check("qb_route_hist_hi_next",
+           lib.qb_route_hist_hi_next(_ptr(logits), _dtype(logits), _ptr(bias), N, E, int(k),
+                                     _ptr(hist_hi), _ptr(keys_out), _ptr(topk_out),
+                                     _ptr(alpha_out), _stream(stream)))
 
 
 def qb_select_hi(hist_hi, r, sel, r_lo, stream=None):
@@ -290,9 +301,15 @@ def eqb_global_batch(microbatches, bias, k, state: EQBState | None = None, keys=
     if bias_out is None:
         bias_out = torch.empty_like(bias)
     row = 0
+    first = True
     for m in microbatches:
         n = int(m.shape[0])
-        qb_route_hist_hi(m, bias, k, state.hist_hi, keys_out=keys[row:row + n], stream=stream)
+        if n == 0:
+            continue  # issues no work
+        # every microbatch after the first continues the batch on this stream
+        route = qb_route_hist_hi if first else qb_route_hist_hi_next
+        route(m, bias, k, state.hist_hi, keys_out=keys[row:row + n], stream=stream)
+        first = False
         row += n
     r = rank(n_pool, E, k)
     qb_select_hi(state.hist_hi, r, state.sel, state.r_lo, stream=stream)

@@ -111,6 +111,21 @@ int qb_route_hist_hi(const void* logits, int dtype, const float* bias, int64_t N
                      int32_t* hist_hi, uint16_t* keys_out, int32_t* topk_out, float* alpha_out,
                      void* stream);
 
+/* A further microbatch of the same global batch: the same operation and
+ * arguments as qb_route_hist_hi, for a call issued on `stream` directly after
+ * a qb_route_hist_hi or qb_route_hist_hi_next call of the same batch (same
+ * bias and hist_hi; [QB-PR] "Implementation": the histogram accumulates over
+ * every microbatch).  At E = 256 the call may start while the one before it
+ * still runs (its counts only add to hist_hi), so back-to-back microbatch
+ * calls overlap instead of each waiting for the last one to finish.
+ * Ownership and ordering: nothing between the two calls on the stream, and no
+ * other stream, may write this call's logits, bias or hist_hi while it runs,
+ * nor read its outputs before the stream reaches a later operation (which
+ * orders after both calls).  Other E: the same as qb_route_hist_hi. */
+int qb_route_hist_hi_next(const void* logits, int dtype, const float* bias, int64_t N, int E,
+                          int k, int32_t* hist_hi, uint16_t* keys_out, int32_t* topk_out,
+                          float* alpha_out, void* stream);
+
 /* Select the hi-byte bin that holds the rank-r value of every expert
  * ([EQB] EQB paragraph: "locate the bin holding the r-th smallest value").
  *   hist_hi  device int32 [E, 256], pooled over the whole global batch.

@@ -60,25 +60,26 @@ def test_argument_errors_are_reported_before_launch(lib):
     fake = ctypes.c_void_p(0x10000)   # 16-byte aligned, never dereferenced
     odd = ctypes.c_void_p(0x10004)
     N0 = None
-    # null logits / bias / histogram
-    assert L.qb_route_hist_hi(N0, 0, fake, 10, 256, 6, fake, N0, N0, N0, N0) == lib.QB_EINVAL
-    assert L.qb_route_hist_hi(fake, 0, N0, 10, 256, 6, fake, N0, N0, N0, N0) == lib.QB_EINVAL
-    assert L.qb_route_hist_hi(fake, 0, fake, 10, 256, 6, N0, N0, N0, N0, N0) == lib.QB_EINVAL
-    # misaligned logits or keys
-    assert L.qb_route_hist_hi(odd, 0, fake, 10, 256, 6, fake, N0, N0, N0, N0) == lib.QB_EINVAL
-    assert L.qb_route_hist_hi(fake, 0, fake, 10, 256, 6, fake, odd, N0, N0, N0) == lib.QB_EINVAL
-    # bad dtype, negative N, N beyond int32 counts
-    assert L.qb_route_hist_hi(fake, 7, fake, 10, 256, 6, fake, N0, N0, N0, N0) == lib.QB_EINVAL
-    assert L.qb_route_hist_hi(fake, 0, fake, -1, 256, 6, fake, N0, N0, N0, N0) == lib.QB_EINVAL
-    assert L.qb_route_hist_hi(fake, 0, fake, 1 << 31, 256, 6, fake, N0, N0, N0, N0) == lib.QB_EOVERFLOW
-    # unsupported E, bad k
-    for E in (0, 16, 48, 1056, 2048):
-        assert L.qb_route_hist_hi(fake, 0, fake, 10, E, 6, fake, N0, N0, N0, N0) == lib.QB_EUNSUPPORTED
-    assert L.qb_route_hist_hi(fake, 0, fake, 10, 256, 0, fake, N0, N0, N0, N0) == lib.QB_EINVAL
-    assert L.qb_route_hist_hi(fake, 0, fake, 10, 32, 32, fake, N0, N0, N0, N0) == lib.QB_EINVAL
-    assert L.qb_route_hist_hi(fake, 0, fake, 10, 256, 16, fake, N0, N0, N0, N0) == lib.QB_EUNSUPPORTED
-    # empty input is a no-op
-    assert L.qb_route_hist_hi(fake, 0, fake, 0, 256, 6, fake, N0, N0, N0, N0) == lib.QB_OK
+    for hi in (L.qb_route_hist_hi, L.qb_route_hist_hi_next):
+        # null logits / bias / histogram
+        assert hi(N0, 0, fake, 10, 256, 6, fake, N0, N0, N0, N0) == lib.QB_EINVAL
+        assert hi(fake, 0, N0, 10, 256, 6, fake, N0, N0, N0, N0) == lib.QB_EINVAL
+        assert hi(fake, 0, fake, 10, 256, 6, N0, N0, N0, N0, N0) == lib.QB_EINVAL
+        # misaligned logits or keys
+        assert hi(odd, 0, fake, 10, 256, 6, fake, N0, N0, N0, N0) == lib.QB_EINVAL
+        assert hi(fake, 0, fake, 10, 256, 6, fake, odd, N0, N0, N0) == lib.QB_EINVAL
+        # bad dtype, negative N, N beyond int32 counts
+        assert hi(fake, 7, fake, 10, 256, 6, fake, N0, N0, N0, N0) == lib.QB_EINVAL
+        assert hi(fake, 0, fake, -1, 256, 6, fake, N0, N0, N0, N0) == lib.QB_EINVAL
+        assert hi(fake, 0, fake, 1 << 31, 256, 6, fake, N0, N0, N0, N0) == lib.QB_EOVERFLOW
+        # unsupported E, bad k
+        for E in (0, 16, 48, 1056, 2048):
+            assert hi(fake, 0, fake, 10, E, 6, fake, N0, N0, N0, N0) == lib.QB_EUNSUPPORTED
+        assert hi(fake, 0, fake, 10, 256, 0, fake, N0, N0, N0, N0) == lib.QB_EINVAL
+        assert hi(fake, 0, fake, 10, 32, 32, fake, N0, N0, N0, N0) == lib.QB_EINVAL
+        assert hi(fake, 0, fake, 10, 256, 16, fake, N0, N0, N0, N0) == lib.QB_EUNSUPPORTED
+        # empty input is a no-op
+        assert hi(fake, 0, fake, 0, 256, 6, fake, N0, N0, N0, N0) == lib.QB_OK
     # select: rank out of range
     assert L.qb_select_hi(fake, 256, 0, fake, fake, N0) == lib.QB_EINVAL
     assert L.qb_select_hi(fake, 256, 1 << 31, fake, fake, N0) == lib.QB_EOVERFLOW

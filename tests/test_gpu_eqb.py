@@ -107,15 +107,17 @@ def test_route_margins_outside_shared_window(qb, orc):
     assert h[:, ~inside].sum() > 0
 
 
-def _eqb_gpu(qb, mbs, bias, k):
+def _eqb_gpu(qb, mbs, bias, k, chained=False):
+    # chained: every microbatch call after the first is qb_route_hist_hi_next
     E = bias.shape[0]
     st = qb.EQBState(E, bias.device)
     n_pool = sum(m.shape[0] for m in mbs)
     keys = torch.empty(n_pool, E, dtype=torch.int16, device=bias.device)
     b_out = torch.empty_like(bias)
     row = 0
-    for m in mbs:
-        qb.qb_route_hist_hi(m, bias, k, st.hist_hi, keys_out=keys[row:row + m.shape[0]])
+    for i, m in enumerate(mbs):
+        route = qb.qb_route_hist_hi_next if chained and i > 0 else qb.qb_route_hist_hi
+        route(m, bias, k, st.hist_hi, keys_out=keys[row:row + m.shape[0]])
         row += m.shape[0]
     r = qb.rank(n_pool, E, k)
     qb.qb_select_hi(st.hist_hi, r, st.sel, st.r_lo)
@@ -152,11 +154,13 @@ def test_eqb_pooled_workload_and_partition_invariance(qb, orc):
     ref = orc.eqb_global_batch([host_logits(m) for m in mbs], bias.cpu().numpy(), w.k)
     _check_eqb(res, ref)
     allx = torch.cat(mbs)
-    for n_m, n_t in ((2, 65536), (32, 4096), (1, 131072)):
+    for n_m, n_t, chained in ((2, 65536, False), (32, 4096, False), (1, 131072, False),
+                              (8, 16384, True), (32, 4096, True), (128, 1024, True)):
         parts = [allx[i * n_t:(i + 1) * n_t] for i in range(n_m)]
-        other = _eqb_gpu(qb, parts, bias, w.k)
+        other = _eqb_gpu(qb, parts, bias, w.k, chained=chained)
         for key in ("hist_hi", "hist_lo", "sel", "r_lo", "qkey", "bias_out"):
-            assert np.array_equal(res[key], other[key]), (n_m, key)
+            assert np.array_equal(res[key], other[key]), (n_m, chained, key)
+        assert torch.equal(res["keys"], other["keys"]), (n_m, chained)
     # rank-local (per-microbatch) histograms differ before pooling
     h0 = gpu_route(qb, mbs[0], bias, w.k)["hist_hi"]
     h1 = gpu_route(qb, mbs[1], bias, w.k)["hist_hi"]
@@ -192,6 +196,32 @@ def test_reset_in_place_and_replay_counted_once(qb, orc):
     assert np.array_equal(st.hist_hi.cpu().numpy(), once)
 
 
+@pytest.mark.parametrize("E,dtype", [(256, torch.float32), (256, torch.bfloat16),
+                                     (64, torch.float32)])
+def test_chained_microbatches_across_steps(qb, orc, E, dtype):
+    # Two global batches back to back on one stream through the binding's
+    # helper, whose microbatch calls after the first are qb_route_hist_hi_next.
+    # The second batch routes with the bias that the first batch's finalize
+    # wrote, on the histogram it reset: a chained call that ran ahead of the
+    # finalize would change the second bias.
+    w = inputs.scaled(inputs.WORKLOADS["eqb_pooled"], E=E, n_micro=6, n_tokens=5000,
+                      logits_dtype=dtype)
+    bias, mbs1 = inputs.router_layer(w, 91, device="cuda")
+    _, mbs2 = inputs.router_layer(w, 92, device="cuda")
+    st = qb.EQBState(E, bias.device)
+    keys = torch.empty(w.n_pool, E, dtype=torch.int16, device="cuda")
+    b1, b2 = torch.empty_like(bias), torch.empty_like(bias)
+    qb.eqb_global_batch(mbs1, bias, w.k, state=st, keys=keys, bias_out=b1)
+    qb.eqb_global_batch(mbs2, b1, w.k, state=st, keys=keys, bias_out=b2)
+    torch.cuda.synchronize()
+    assert qb.device_status() == 0
+    ref1 = orc.eqb_global_batch([host_logits(m) for m in mbs1], bias.cpu().numpy(), w.k)
+    ref2 = orc.eqb_global_batch([host_logits(m) for m in mbs2], ref1["bias_out"], w.k)
+    assert np.array_equal(b1.cpu().numpy().view(np.uint32), ref1["bias_out"].view(np.uint32))
+    assert np.array_equal(b2.cpu().numpy().view(np.uint32), ref2["bias_out"].view(np.uint32))
+    assert np.array_equal(np_u16(keys), np.concatenate(ref2["keys"]))
+
+
 @pytest.mark.parametrize("layer", [0, 23, 47])
 def test_full_step_layer_at_bench_size(qb, orc, layer):
     # Layers 0, 23 and 47 of the full-step workload (their own seeds), each
@@ -203,8 +233,8 @@ def test_full_step_layer_at_bench_size(qb, orc, layer):
     bias, mbs = inputs.router_layer(w, inputs.seed_for("full_step", layer), device="cuda",
                                     out=out)
     ref = orc.eqb_global_batch([out.cpu().numpy()], bias.cpu().numpy(), w.k)
-    for parts in (mbs, [out]):
-        res = _eqb_gpu(qb, parts, bias, w.k)
+    for parts, chained in ((mbs, False), (mbs, True), ([out], False)):
+        res = _eqb_gpu(qb, parts, bias, w.k, chained=chained)
         _check_eqb(res, ref)
         assert np.array_equal(np_u16(res["keys"]), np.concatenate(ref["keys"]))
 

@@ -42,7 +42,7 @@ METRIC = "QB routed tokens/s per layer (E=256,k=6, 2-pass EQB) on 1 GB300; % of 
 # launch (route256_kernel, keys written, no top-k output) on a 524288-token
 # layer, from an ncu capture of that launch.  Reported only while the
 # kernel's sources hash to the value they had when the counters were taken.
-ROUTE_TRAFFIC = {"sha1": "b8e4a23db07499146b46306e3303ed5c8c5f8875", "tokens": 524288,
+ROUTE_TRAFFIC = {"sha1": "83b7131cae884c76307c70dca5155d0d448a1fd3", "tokens": 524288,
                  "bytes": (537.004288 + 232.871424) * 1e6}
 ROUTE_SOURCES = ("qb_route256.cuh", "qb_route256_f32.cu", "qb_route.cuh", "qb_device.cuh")
 # Warp instructions of the same capture (smsp__inst_executed.sum), for the
@@ -52,7 +52,7 @@ ROUTE_INSTR = {"tokens": 524288, "warp_instructions": 127038039}
 # bf16 tokens: the alpha pass (route256_kernel, K3 mode) plus the count
 # kernel, from an ncu capture of those launches; reported while the K3
 # sources hash to the value they had when it was taken.
-K3_INSTR = {"sha1": "a53c74cba5b2efff6e4e3aa06b44b4c2b4c74dcc", "tokens": 65536,
+K3_INSTR = {"sha1": "23acfde26fd7c08ed6a8a7cf73173389ccadb1c8", "tokens": 65536,
             "warp_instructions": 12850624 + 13192792}
 K3_SOURCES = ("qb_route256.cuh", "qb_route256_bf16.cu", "qb_route.cuh", "qb_device.cuh",
               "qb_k3.cu")

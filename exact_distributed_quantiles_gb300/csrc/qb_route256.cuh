@@ -714,7 +714,8 @@ __global__ void __launch_bounds__(warps_max(MODE) * 32, 1) route256_kernel(const
   if (!a.chained) asm volatile("griddepcontrol.wait;" ::: "memory");
   // From here on, a kernel launched as this one's programmatic dependent (the
   // next chained call, or lei_apply_overlap) may take the room this CTA
-  // leaves: everything before this kernel has completed.
+  // leaves: everything before this kernel has completed, except the earlier
+  // hi passes of a chain, which only add to the histogram.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int i = threadIdx.x; i < kE; i += blockDim.x) bias_s[i] = a.bias[i];
   if (lane == 0) {

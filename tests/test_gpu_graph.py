@@ -71,3 +71,52 @@ def test_layer_replayed_from_a_graph_equals_direct_calls(qb):
     assert torch.equal(bias.view(torch.int32), bias_direct.view(torch.int32))
     assert torch.equal(grad.view(torch.int32), grad_direct.view(torch.int32))
     assert int(hi.abs().sum()) == 0 and int(lo.abs().sum()) == 0  # reset in place
+
+
+def test_chained_microbatch_calls_replayed_from_a_graph(qb):
+    # The microbatch calls after the first are qb_route_hist_hi_next, whose
+    # programmatic dependencies become graph edges; three replays of the
+    # captured global batch (each routing with the bias the one before wrote)
+    # equal three direct runs.
+    w = inputs.scaled(inputs.WORKLOADS["full_step"], n_micro=8, n_tokens=8192)
+    n, E, k = w.n_pool, w.E, w.k
+    logits = torch.empty(n, E, dtype=torch.float32, device="cuda")
+    bias0, mbs = inputs.router_layer(w, inputs.seed_for("full_step", 5), device="cuda",
+                                     out=logits)
+    bias = bias0.clone()
+    hi = torch.zeros(E, 256, dtype=torch.int32, device="cuda")
+    lo = torch.zeros_like(hi)
+    sel = torch.empty(E, dtype=torch.int32, device="cuda")
+    r_lo = torch.empty_like(sel)
+    keys = torch.empty(n, E, dtype=torch.int16, device="cuda")
+    R = qb.rank(n, E, k)
+
+    def batch():
+        for m, x in enumerate(mbs):
+            route = qb.qb_route_hist_hi if m == 0 else qb.qb_route_hist_hi_next
+            route(x, bias, k, hi, keys_out=keys[m * w.n_tokens:(m + 1) * w.n_tokens])
+        qb.qb_select_hi(hi, R, sel, r_lo)
+        qb.qb_keys_hist_lo(keys, sel, lo)
+        qb.qb_finalize(hi, lo, sel, r_lo, bias, reset=True)
+
+    direct = []
+    for _ in range(3):
+        batch()
+        direct.append(bias.clone())
+    torch.cuda.synchronize()
+    assert qb.device_status() == 0
+
+    bias.copy_(bias0)
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            batch()
+    torch.cuda.current_stream().wait_stream(s)
+    for step in range(3):
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(bias.view(torch.int32), direct[step].view(torch.int32)), step
+    assert qb.device_status() == 0
+    assert int(hi.abs().sum()) == 0 and int(lo.abs().sum()) == 0

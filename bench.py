@@ -402,25 +402,26 @@ def gemm_component(qb, inputs, dev, reps, warmup, peak_hbm, peaks):
         for h in hs:
             qb.qb_router_gemm(h, w_t, logits5)
 
-    def gemm_batch():
+    def fused_calls(chained=True):
+        # the fused path: logits stay in tensor memory (no logits_out); the
+        # microbatches after the first continue the batch (..._next)
         for i, h in enumerate(hs):
-            # the fused path: logits stay in tensor memory (no logits_out)
-            qb.qb_router_gemm_hist_hi(h, w_t, b5, w5.k, None, hi5,
-                                      keys_out=keys5[i * n:(i + 1) * n])
+            f = qb.qb_router_gemm_hist_hi_next if chained and i else qb.qb_router_gemm_hist_hi
+            f(h, w_t, b5, w5.k, None, hi5, keys_out=keys5[i * n:(i + 1) * n])
+
+    def gemm_batch():
+        fused_calls()
         qb.qb_select_hi(hi5, R5, sel5, rlo5)
         qb.qb_keys_hist_lo(keys5, sel5, lo5)
         qb.qb_finalize(hi5, lo5, sel5, rlo5, b5, reset=True)
 
-    def fused_only():
-        for i, h in enumerate(hs):
-            qb.qb_router_gemm_hist_hi(h, w_t, b5, w5.k, None, hi5,
-                                      keys_out=keys5[i * n:(i + 1) * n])
-
     # CUDA graphs of each call shape (device times, not the host's launch rate)
     ms5 = _per_call_ms(_graph(gemm_batch), reps, warmup)
     ms_g = _per_call_ms(_graph(gemm_only), reps, warmup)
-    # per microbatch, the 4 microbatches in turn (none of them in L2)
-    ms_f = _per_call_ms(_graph(fused_only), reps, warmup) / len(hs)
+    # per microbatch, the 4 microbatches in turn (none of them in L2); and
+    # with every call waiting for the one before it
+    ms_f = _per_call_ms(_graph(fused_calls), reps, warmup) / len(hs)
+    ms_fw = _per_call_ms(_graph(lambda: fused_calls(False)), reps, warmup) / len(hs)
     qb.qb_zero_i32(hi5)
     flops = 2.0 * w5.n_pool * H * E
     gbytes = w5.n_pool * H * 2 + H * E * 2 * w5.n_micro + w5.n_pool * E * 4
@@ -444,6 +445,7 @@ def gemm_component(qb, inputs, dev, reps, warmup, peak_hbm, peaks):
         "value": w5.n_pool / (ms5 / 1e3), "unit": "tokens/s", "ms_per_batch": ms5,
         "launches_per_batch": w5.n_micro + 3,
         "fused_ms_per_microbatch": ms_f,
+        "fused_ms_per_microbatch_each_waiting": ms_fw,
         "roofline": {"bound": "hbm" if f_hbm_bound else "tensor",
                      "kernel": "gemm_route_kernel (tcgen05 GEMM + hi pass in the epilogue; "
                                "keys written, logits kept in tensor memory)",

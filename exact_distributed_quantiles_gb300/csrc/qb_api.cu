@@ -67,6 +67,33 @@ int check_route_args(const void* logits, int dtype, const float* bias, int64_t N
   return QB_OK;
 }
 
+int router_gemm_hist_hi(const void* hidden, const void* w_t, int64_t M, int H, int E, int k,
+                        const float* bias, float* logits_out, int32_t* hist_hi,
+                        uint16_t* keys_out, int32_t* topk_out, float* alpha_out, void* stream,
+                        bool chained) {
+  if (!hidden || !w_t || !bias || !hist_hi) return QB_EINVAL;
+  if (!aligned16(hidden) || !aligned16(w_t)) return QB_EINVAL;
+  if ((logits_out && !aligned16(logits_out)) || (keys_out && !aligned16(keys_out)))
+    return QB_EINVAL;
+  if (M < 0) return QB_EINVAL;
+  if (M > INT32_MAX) return QB_EOVERFLOW;
+  if (E < 32 || E > 256 || E % 32 != 0 || H < 64 || H % 64 != 0) return QB_EUNSUPPORTED;
+  if (k < 1 || k >= E) return QB_EINVAL;
+  if (k > 15) return QB_EUNSUPPORTED;
+  if (E != 256 && !logits_out) return QB_EUNSUPPORTED;
+  if (M == 0) return QB_OK;
+  if (E == 256)
+    return launch_router_gemm_route(hidden, w_t, M, H, k, bias, hist_hi, keys_out, topk_out,
+                                    alpha_out, logits_out, as_stream(stream), chained);
+  // Other expert counts: the plain GEMM into logits_out, then the routing
+  // pass on those logits (two launches; the fused epilogue is built for 256
+  // experts).  The results are the same: the fused kernel equals the routing
+  // pass run on its own logits.
+  int st = launch_router_gemm(hidden, w_t, M, H, E, logits_out, as_stream(stream));
+  if (st != QB_OK) return st;
+  return launch_route_hi(logits_out, QB_F32, bias, M, E, k, hist_hi, keys_out, topk_out,
+                         alpha_out, nullptr, nullptr, 0, as_stream(stream));
+}
 }  // namespace
 
 extern "C" {
@@ -78,7 +105,7 @@ const char* qb_status_string(int status) {
     case QB_EINVAL:
       return "invalid argument (null or misaligned pointer, bad size or rank)";
     case QB_EUNSUPPORTED:
-      return "unsupported E or k (E in {32,64,128,256,512}, 1 <= k <= 15, k < E)";
+      return "unsupported E or k (E a multiple of 32 up to 1024, 1 <= k <= 15, k < E)";
     case QB_ECUDA:
       return "CUDA launch or runtime error";
     case QB_EOVERFLOW:
@@ -286,28 +313,16 @@ int qb_router_gemm_hist_hi(const void* hidden, const void* w_t, int64_t M, int H
                            const float* bias, float* logits_out, int32_t* hist_hi,
                            uint16_t* keys_out, int32_t* topk_out, float* alpha_out,
                            void* stream) {
-  if (!hidden || !w_t || !bias || !hist_hi) return QB_EINVAL;
-  if (!aligned16(hidden) || !aligned16(w_t)) return QB_EINVAL;
-  if ((logits_out && !aligned16(logits_out)) || (keys_out && !aligned16(keys_out)))
-    return QB_EINVAL;
-  if (M < 0) return QB_EINVAL;
-  if (M > INT32_MAX) return QB_EOVERFLOW;
-  if (E < 32 || E > 256 || E % 32 != 0 || H < 64 || H % 64 != 0) return QB_EUNSUPPORTED;
-  if (k < 1 || k >= E) return QB_EINVAL;
-  if (k > 15) return QB_EUNSUPPORTED;
-  if (E != 256 && !logits_out) return QB_EUNSUPPORTED;
-  if (M == 0) return QB_OK;
-  if (E == 256)
-    return launch_router_gemm_route(hidden, w_t, M, H, k, bias, hist_hi, keys_out, topk_out,
-                                    alpha_out, logits_out, as_stream(stream));
-  // Other expert counts: the plain GEMM into logits_out, then the routing
-  // pass on those logits (two launches; the fused epilogue is built for 256
-  // experts).  The results are the same: the fused kernel equals the routing
-  // pass run on its own logits.
-  int st = launch_router_gemm(hidden, w_t, M, H, E, logits_out, as_stream(stream));
-  if (st != QB_OK) return st;
-  return launch_route_hi(logits_out, QB_F32, bias, M, E, k, hist_hi, keys_out, topk_out,
-                         alpha_out, nullptr, nullptr, 0, as_stream(stream));
+  return router_gemm_hist_hi(hidden, w_t, M, H, E, k, bias, logits_out, hist_hi, keys_out,
+                             topk_out, alpha_out, stream, false);
+}
+
+int qb_router_gemm_hist_hi_next(const void* hidden, const void* w_t, int64_t M, int H, int E,
+                                int k, const float* bias, float* logits_out, int32_t* hist_hi,
+                                uint16_t* keys_out, int32_t* topk_out, float* alpha_out,
+                                void* stream) {
+  return router_gemm_hist_hi(hidden, w_t, M, H, E, k, bias, logits_out, hist_hi, keys_out,
+                             topk_out, alpha_out, stream, true);
 }
 
 int qb_rank_average(const uint16_t* qkeys, int P, int E, float* bias_out, void* stream) {

@@ -78,6 +78,10 @@ struct FusedArgs {
   float* alpha_out;    // [M] or null
   float* logits_out;   // [M, 256] or null
   int* status;
+  // a later microbatch of the same global batch, issued right after another
+  // fused call on the stream (qb_router_gemm_hist_hi_next): skips the wait
+  // for the previous kernel at its start and waits at its end instead
+  int chained;
 };
 
 // The window slot of a hi byte computed in registers (the same map as the
@@ -125,7 +129,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   for (int i = threadIdx.x; i < kWinSlots * kWinRow; i += blockDim.x) win[i] = 0;
   for (int i = threadIdx.x; i < 256; i += blockDim.x) lut[i] = (uint8_t)route::window_slot_of(i);
-  for (int i = threadIdx.x; i < kE; i += blockDim.x) bias_s[i] = g.bias[i];
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full + s, 1);
@@ -137,6 +140,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_mbar_init();
   }
+  // Launched as a programmatic dependent of the kernel before it: wait for
+  // its completion (and its memory) before the first global read and before
+  // taking tensor memory.  A chained call follows another fused call of the
+  // same global batch that has itself waited (its counts only add to the
+  // same histogram, its outputs are other rows), so it goes on at once and
+  // waits at its end instead, so that it completes after the call before it.
+  // The next chained call may launch from here on; one CTA fills an SM
+  // (shared memory), so its CTAs take SMs as this call's CTAs leave them.
+  if (!g.chained) asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  for (int i = threadIdx.x; i < kE; i += blockDim.x) bias_s[i] = g.bias[i];
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 2 * kE);
   tc_fence_before();
   __syncthreads();
@@ -471,6 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 2 * kE);
   }
+  if (g.chained) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 int64_t grid_of(int64_t M) {
@@ -483,14 +498,27 @@ template <int KL, int K1>
 int launch_fused(const CUtensorMap& ma, const CUtensorMap& mb, const FusedArgs& g,
                  cudaStream_t stream) {
   auto kern = gemm_route_kernel<KL, K1>;
-  static bool attr = false;  // per instantiation; benign race (idempotent)
-  if (!attr) {
+  static bool attr_set = false;  // per instantiation; benign race (idempotent)
+  if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
         cudaSuccess)
       return launch_status();
-    attr = true;
+    attr_set = true;
   }
-  kern<<<(unsigned)grid_of(g.M), kThreads, kSmemBytes, stream>>>(ma, mb, g);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid_of(g.M));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, ma, mb, g) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return QB_ECUDA;
+  }
   return launch_status();
 }
 
@@ -499,7 +527,7 @@ int launch_fused(const CUtensorMap& ma, const CUtensorMap& mb, const FusedArgs& 
 int launch_router_gemm_route(const void* hidden, const void* w_t, int64_t M, int K, int k,
                              const float* bias, int32_t* hist, uint16_t* keys_out,
                              int32_t* topk_out, float* alpha_out, float* logits_out,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, bool chained) {
   if (K % kBK != 0 || K <= 0) return QB_EUNSUPPORTED;
   int* status = device_status_ptr();
   if (!status) return QB_ECUDA;
@@ -513,10 +541,11 @@ int launch_router_gemm_route(const void* hidden, const void* w_t, int64_t M, int
                               (uint64_t)m, (uint64_t)K, kBM))
       return QB_EINVAL;
     if (!make_bf16_kmajor_map(&mb, w_t, (uint64_t)kE, (uint64_t)K, kE)) return QB_EINVAL;
+    // every launch after the first of a call continues the same batch
     FusedArgs g{bias, m, K, k, hist,
                 keys_out ? keys_out + off * kE : nullptr, topk_out ? topk_out + off * k : nullptr,
                 alpha_out ? alpha_out + off : nullptr, logits_out ? logits_out + off * kE : nullptr,
-                status};
+                status, (chained || off > 0) ? 1 : 0};
     int st;
     if (k + 1 == 7)
       st = launch_fused<8, 7>(ma, mb, g, stream);

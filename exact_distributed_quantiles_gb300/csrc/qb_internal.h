@@ -65,7 +65,7 @@ int launch_wait_timeout_selftest(uint32_t polls, cudaStream_t stream);
 int launch_router_gemm_route(const void* hidden, const void* w_t, int64_t M, int K, int k,
                              const float* bias, int32_t* hist, uint16_t* keys_out,
                              int32_t* topk_out, float* alpha_out, float* logits_out,
-                             cudaStream_t stream);
+                             cudaStream_t stream, bool chained = false);
 int launch_rank_average(const uint16_t* qkeys, int P, int E, float* bias_out,
                         cudaStream_t stream);
 int launch_maxvio(const int32_t* topk, int64_t N, int E, int k, int64_t batch_tokens,

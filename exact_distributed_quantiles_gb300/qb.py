@@ -24,7 +24,8 @@ EXPORTS = ("qb_status_string", "qb_version", "qb_rank", "qb_sigmoid", "qb_sigmoi
            "qb_route_hist_hi", "qb_route_hist_hi_next", "qb_select_hi", "qb_keys_hist_lo",
            "qb_route_hist_lo",
            "qb_finalize", "k3_route_hist", "k3_finalize", "lei_inject", "qb_device_status",
-           "lei_inject_noalloc", "qb_router_gemm", "qb_router_gemm_hist_hi", "qb_rank_average",
+           "lei_inject_noalloc", "qb_router_gemm", "qb_router_gemm_hist_hi",
+           "qb_router_gemm_hist_hi_next", "qb_rank_average",
            "qb_maxvio", "lei_rho", "lei_apply",
            "lei_apply_overlap", "qb_selftest_wait_timeout")
 
@@ -61,6 +62,7 @@ def _load():
         "lei_inject_noalloc": (I, [P, P, I64, I, I, F, I64, P]),
         "qb_router_gemm": (I, [P, P, I64, I, I, P, P]),
         "qb_router_gemm_hist_hi": (I, [P, P, I64, I, I, I, P, P, P, P, P, P, P]),
+        "qb_router_gemm_hist_hi_next": (I, [P, P, I64, I, I, I, P, P, P, P, P, P, P]),
         "qb_rank_average": (I, [P, I, I, P, P]),
         "qb_maxvio": (I, [P, I64, I, I, I64, P, P, P]),
         "lei_rho": (I, [P, I64, I, I, F, I64, P, P]),
@@ -248,6 +250,16 @@ def qb_router_gemm_hist_hi(hidden, w_t, bias, k, logits_out, hist_hi, keys_out=N
            lib.qb_router_gemm_hist_hi(_ptr(hidden), _ptr(w_t), M, H, E, int(k), _ptr(bias),
                                       _ptr(logits_out), _ptr(hist_hi), _ptr(keys_out),
                                       _ptr(topk_out), _ptr(alpha_out), _stream(stream)))
+
+
+def qb_router_gemm_hist_hi_next(hidden, w_t, bias, k, logits_out, hist_hi, keys_out=None,
+                                topk_out=None, alpha_out=None, stream=None):
+    M, H = hidden.shape
+    E = w_t.shape[0]
+    _check("qb_router_gemm_hist_hi_next",
+           lib.qb_router_gemm_hist_hi_next(_ptr(hidden), _ptr(w_t), M, H, E, int(k), _ptr(bias),
+                                           _ptr(logits_out), _ptr(hist_hi), _ptr(keys_out),
+                                           _ptr(topk_out), _ptr(alpha_out), _stream(stream)))
 
 
 def qb_rank_average(qkeys, bias_out, stream=None):

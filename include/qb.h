@@ -282,6 +282,19 @@ int qb_router_gemm_hist_hi(const void* hidden, const void* w_t, int64_t M, int H
                            uint16_t* keys_out, int32_t* topk_out, float* alpha_out,
                            void* stream);
 
+/* A further microbatch of the same global batch: the same operation and
+ * arguments as qb_router_gemm_hist_hi, for a call issued on `stream`
+ * directly after a qb_router_gemm_hist_hi or qb_router_gemm_hist_hi_next
+ * call of the same batch (same bias and hist_hi).  At E = 256 the call's CTAs
+ * may start on the SMs that the previous call's CTAs leave while its last
+ * tiles are still in their epilogues; the ownership and ordering rules are
+ * those of qb_route_hist_hi_next.  Other E: the same as
+ * qb_router_gemm_hist_hi. */
+int qb_router_gemm_hist_hi_next(const void* hidden, const void* w_t, int64_t M, int H, int E,
+                                int k, const float* bias, float* logits_out, int32_t* hist_hi,
+                                uint16_t* keys_out, int32_t* topk_out, float* alpha_out,
+                                void* stream);
+
 /* Load-error injection without a caller workspace.  The pages have no
  * counterpart to this entry point; it exists for callers that cannot allocate
  * device memory where LEI is applied -- code under a framework whose caching

@@ -120,6 +120,17 @@ def test_argument_errors_are_reported_before_launch(lib):
     assert L.lei_apply_overlap(fake, 10, 256, -1, fake, N0) == lib.QB_EINVAL
     assert L.lei_apply_overlap(fake, 10, 48, 0, fake, N0) == lib.QB_EUNSUPPORTED
     assert L.lei_apply_overlap(fake, 0, 256, 0, fake, N0) == lib.QB_OK
+    # router GEMM with the hi pass (plain and chained entries)
+    for g in (L.qb_router_gemm_hist_hi, L.qb_router_gemm_hist_hi_next):
+        assert g(N0, fake, 10, 2048, 256, 6, fake, N0, fake, N0, N0, N0, N0) == lib.QB_EINVAL
+        assert g(odd, fake, 10, 2048, 256, 6, fake, N0, fake, N0, N0, N0, N0) == lib.QB_EINVAL
+        assert g(fake, fake, 10, 2048, 256, 6, fake, N0, N0, N0, N0, N0, N0) == lib.QB_EINVAL
+        assert g(fake, fake, 10, 2000, 256, 6, fake, N0, fake, N0, N0, N0, N0) == lib.QB_EUNSUPPORTED
+        assert g(fake, fake, 10, 2048, 288, 6, fake, fake, fake, N0, N0, N0, N0) == lib.QB_EUNSUPPORTED
+        assert g(fake, fake, 10, 2048, 96, 6, fake, N0, fake, N0, N0, N0, N0) == lib.QB_EUNSUPPORTED
+        assert g(fake, fake, 10, 2048, 256, 0, fake, N0, fake, N0, N0, N0, N0) == lib.QB_EINVAL
+        assert g(fake, fake, -1, 2048, 256, 6, fake, N0, fake, N0, N0, N0, N0) == lib.QB_EINVAL
+        assert g(fake, fake, 0, 2048, 256, 6, fake, N0, fake, N0, N0, N0, N0) == lib.QB_OK
     # rank average and MaxVio
     assert L.qb_rank_average(N0, 2, 256, fake, N0) == lib.QB_EINVAL
     assert L.qb_rank_average(fake, 0, 256, fake, N0) == lib.QB_EINVAL

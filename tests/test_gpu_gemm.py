@@ -194,13 +194,15 @@ def test_fused_counts_past_one_launch(qb):
     assert torch.equal(keys_f, keys_r)
 
 
-def test_router_gemm_global_batch_chain(qb, orc):
+@pytest.mark.parametrize("chained", [False, True])
+def test_router_gemm_global_batch_chain(qb, orc, chained):
     # The router-GEMM workload end to end: four 32768-token microbatches of
     # the fused GEMM + hi pass (logits kept in tensor memory), then select,
     # the lo pass over the stored keys and the finalize.  Histograms, selected
     # bins and keys, and the new bias are compared bit for bit with the oracle
     # fed the plain GEMM's fp32 logits, which equal the fused kernel's bit for
-    # bit (test_fused_epilogue_matches_routing_of_its_logits).
+    # bit (test_fused_epilogue_matches_routing_of_its_logits).  chained: the
+    # microbatches after the first through qb_router_gemm_hist_hi_next.
     w = inputs.WORKLOADS["router_gemm"]
     bias, W, hs = inputs.gemm_layer(w, inputs.seed_for("router_gemm"), device="cuda")
     w_t = W.t().contiguous()
@@ -208,8 +210,8 @@ def test_router_gemm_global_batch_chain(qb, orc):
     st = qb.EQBState(E, "cuda")
     keys = torch.empty(w.n_pool, E, dtype=torch.int16, device="cuda")
     for i, h in enumerate(hs):
-        qb.qb_router_gemm_hist_hi(h, w_t, bias, w.k, None, st.hist_hi,
-                                  keys_out=keys[i * n:(i + 1) * n])
+        f = qb.qb_router_gemm_hist_hi_next if chained and i else qb.qb_router_gemm_hist_hi
+        f(h, w_t, bias, w.k, None, st.hist_hi, keys_out=keys[i * n:(i + 1) * n])
     hist_hi = st.hist_hi.clone()
     qb.qb_select_hi(st.hist_hi, qb.rank(w.n_pool, E, w.k), st.sel, st.r_lo)
     qb.qb_keys_hist_lo(keys, st.sel, st.hist_lo)

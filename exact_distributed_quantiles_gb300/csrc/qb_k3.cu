@@ -75,10 +75,19 @@ __device__ __forceinline__ void load8x(const __nv_bfloat16* p, float (&x)[8]) {
 // bins of different experts fall in different banks).  GLOBAL: the slice
 // would not fit shared memory, so every count is a global atomic.  Non-zero
 // shared counters are added to the global histogram once at the end.
+// alpha is the output of the kernel this one depends on: read with a plain
+// load issued after the dependency wait (an asm statement, so that the
+// compiler cannot treat it as read-only data and hoist it above the wait).
+__device__ __forceinline__ float ld_after_wait(const float* p) {
+  float v;
+  asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
+
 template <typename T, bool GLOBAL>
 __global__ void __launch_bounds__(kCountThreads, 1)
-    k3_count_kernel(const T* __restrict__ logits, const float* __restrict__ alpha, int64_t N,
-                    int E, const float* __restrict__ bounds, int nbins, int pitch, int bulk,
+    k3_count_kernel(const T* __restrict__ logits, const float* alpha, int64_t N, int E,
+                    const float* bounds, int nbins, int pitch, int bulk,
                     int32_t* __restrict__ hist, int64_t rows_per_cta) {
   extern __shared__ __align__(16) int32_t h[];
   constexpr int kWarps = kCountThreads / 32;
@@ -92,8 +101,13 @@ __global__ void __launch_bounds__(kCountThreads, 1)
   if constexpr (!GLOBAL) {
     for (int i = threadIdx.x; i < kEW * pitch; i += kCountThreads) h[i] = 0;
   }
-  const float lo = bounds[0];
-  const float scale = __fdiv_rn((float)nbins, __fsub_rn(bounds[1], bounds[0]));
+  // Launched as a programmatic dependent of the alpha pass: this CTA may have
+  // cleared its counters while that pass still ran; wait for it (and its
+  // memory) before the first global read.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const float lo = ld_after_wait(bounds);
+  const float hi = ld_after_wait(bounds + 1);
+  const float scale = __fdiv_rn((float)nbins, __fsub_rn(hi, lo));
   const int last = nbins - 1;
   const int chunk = lane & 3;   // experts 8*chunk .. 8*chunk+7 of the slice
   const int rsub = lane >> 2;   // row of the warp's 8
@@ -135,7 +149,7 @@ __global__ void __launch_bounds__(kCountThreads, 1)
   auto load = [&](float (&x)[8], float& a) {
     if (left_l > 0) {
       load8x(pl, x);
-      a = __ldg(pa);
+      a = ld_after_wait(pa);
     }
     --left_l;
     pl += step_l;
@@ -238,8 +252,21 @@ int launch_count_t(const T* logits, const float* alpha, int64_t N, int E, const 
   if (n_tr > max_tr) n_tr = max_tr;
   if (n_tr < 1) n_tr = 1;
   const int64_t rows_per_cta = (N + n_tr - 1) / n_tr;
-  k3_count_kernel<T, GLOBAL><<<(unsigned)(n_tr * n_eg), kCountThreads, smem, stream>>>(
-      logits, alpha, N, E, bounds, nbins, pitch, bulk ? 1 : 0, hist, rows_per_cta);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(n_tr * n_eg));
+  cfg.blockDim = dim3(kCountThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, k3_count_kernel<T, GLOBAL>, logits, alpha, N, E, bounds, nbins,
+                         pitch, bulk ? 1 : 0, hist, rows_per_cta) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return QB_ECUDA;
+  }
   return launch_status();
 }
 

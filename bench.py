@@ -42,8 +42,8 @@ METRIC = "QB routed tokens/s per layer (E=256,k=6, 2-pass EQB) on 1 GB300; % of 
 # launch (route256_kernel, keys written, no top-k output) on a 524288-token
 # layer, from an ncu capture of that launch.  Reported only while the
 # kernel's sources hash to the value they had when the counters were taken.
-ROUTE_TRAFFIC = {"sha1": "83b7131cae884c76307c70dca5155d0d448a1fd3", "tokens": 524288,
-                 "bytes": (537.004288 + 232.871424) * 1e6}
+ROUTE_TRAFFIC = {"sha1": "b37950200c38f8f6fa005644cd04527edcbf9200", "tokens": 524288,
+                 "bytes": (537.040896 + 232.976896) * 1e6}
 ROUTE_SOURCES = ("qb_route256.cuh", "qb_route256_f32.cu", "qb_route.cuh", "qb_device.cuh")
 # Warp instructions of the same capture (smsp__inst_executed.sum), for the
 # issue-rate roofline of this issue-bound kernel; same hash guard.
@@ -52,8 +52,8 @@ ROUTE_INSTR = {"tokens": 524288, "warp_instructions": 127038039}
 # bf16 tokens: the alpha pass (route256_kernel, K3 mode) plus the count
 # kernel, from an ncu capture of those launches; reported while the K3
 # sources hash to the value they had when it was taken.
-K3_INSTR = {"sha1": "ed34ef0113cdfaa15d6c0c4520f72835a2ddf67c", "tokens": 65536,
-            "warp_instructions": 12850624 + 13202520}
+K3_INSTR = {"sha1": "bf0cfb4e3b06c4db6a6ec80c73bba64f29a8be0b", "tokens": 65536,
+            "warp_instructions": 12850624 + 13207384}
 K3_SOURCES = ("qb_route256.cuh", "qb_route256_bf16.cu", "qb_route.cuh", "qb_device.cuh",
               "qb_k3.cu")
 UNIT = "tokens/s/layer"
@@ -342,13 +342,16 @@ def k3_component(qb, inputs, dev, reps, warmup, peak_hbm):
     copies = [[m.clone() for m in mbs3] for _ in range(4)]
     bounds = inputs.k3_initial_bounds(bias3).to(dev)
     hist3 = torch.zeros(w3.E, 1000, dtype=torch.int32, device=dev)
-    alpha3 = torch.empty(w3.n_tokens, dtype=torch.float32, device=dev)
+    # two alpha buffers in turn: a chained call's alpha pass may overlap the
+    # previous call's counting
+    alpha3 = torch.empty(2, w3.n_tokens, dtype=torch.float32, device=dev)
     b3 = bias3.clone()
     R3 = qb.rank(w3.n_pool, w3.E, w3.k)
 
-    def k3_hist_only(c):
-        for m in copies[c]:
-            qb.k3_route_hist(m, b3, w3.k, bounds, hist3, alpha3)
+    def k3_hist_only(c, chained=True):
+        for i, m in enumerate(copies[c]):
+            f = qb.k3_route_hist_next if chained and i else qb.k3_route_hist
+            f(m, b3, w3.k, bounds, hist3, alpha3[i % 2])
 
     def k3_batch(c):
         k3_hist_only(c)
@@ -360,12 +363,15 @@ def k3_component(qb, inputs, dev, reps, warmup, peak_hbm):
                             reps, warmup)
     ms_hist = _per_call_ms(_rotating([_graph(lambda c=c: k3_hist_only(c)) for c in range(4)]),
                            reps, warmup)
+    ms_hist_w = _per_call_ms(_rotating([_graph(lambda c=c: k3_hist_only(c, False))
+                                        for c in range(4)]), reps, warmup)
     qb.qb_zero_i32(hist3)
     k3_bytes = w3.n_pool * w3.E * 2  # bf16 logits read once (algorithmic)
     return {
         "workload": "k3: 4x65536 bf16 tokens, E=256, k=8, 1000 bins",
         "value": w3.n_pool / (ms_batch / 1e3), "unit": "tokens/s", "ms_per_batch": ms_batch,
         "launches_per_batch": 2 * w3.n_micro + 1, "cuda_graph": True,
+        "microbatches_chained": True, "hist_ms_per_batch_each_waiting": ms_hist_w,
         "roofline": {"bound": "hbm", "kernel": "k3_route_hist (route256_kernel alpha pass + k3_count_kernel)",
                      "achieved": k3_bytes / (ms_hist / 1e3) / 1e9, "peak": peak_hbm,
                      "unit": "GB/s", "frac": k3_bytes / (ms_hist / 1e3) / 1e9 / peak_hbm,

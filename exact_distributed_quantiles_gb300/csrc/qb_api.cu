@@ -94,6 +94,26 @@ int router_gemm_hist_hi(const void* hidden, const void* w_t, int64_t M, int H, i
   return launch_route_hi(logits_out, QB_F32, bias, M, E, k, hist_hi, keys_out, topk_out,
                          alpha_out, nullptr, nullptr, 0, as_stream(stream));
 }
+
+int k3_route_hist_impl(const void* logits, int dtype, const float* bias, int64_t N, int E, int k,
+                       const float* bounds, int nbins, int32_t* hist, float* alpha_out,
+                       void* stream, bool chained) {
+  int st = check_route_args(logits, dtype, bias, N, E, k);
+  if (st != QB_OK) return st;
+  if (!bounds || !hist || !alpha_out) return QB_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(alpha_out) & 3u) != 0) return QB_EINVAL;
+  if (nbins < 1 || nbins > 65536) return QB_EINVAL;
+  if (N == 0) return QB_OK;
+  cudaStream_t s = as_stream(stream);
+  if (E == 256)
+    st = dtype == QB_F32 ? launch_route256_alpha_f32(logits, bias, N, k, alpha_out, s, chained)
+                         : launch_route256_alpha_bf16(logits, bias, N, k, alpha_out, s, chained);
+  else
+    st = launch_route_k3(logits, dtype, bias, N, E, k, nullptr, nullptr, nullptr, alpha_out,
+                         nullptr, bounds, nbins, s);
+  if (st != QB_OK) return st;
+  return launch_k3_count(logits, dtype, alpha_out, N, E, bounds, nbins, hist, s);
+}
 }  // namespace
 
 extern "C" {
@@ -217,21 +237,15 @@ int qb_finalize(int32_t* hist_hi, int32_t* hist_lo, const int32_t* sel, const in
 int k3_route_hist(const void* logits, int dtype, const float* bias, int64_t N, int E, int k,
                   const float* bounds, int nbins, int32_t* hist, float* alpha_out,
                   void* stream) {
-  int st = check_route_args(logits, dtype, bias, N, E, k);
-  if (st != QB_OK) return st;
-  if (!bounds || !hist || !alpha_out) return QB_EINVAL;
-  if ((reinterpret_cast<uintptr_t>(alpha_out) & 3u) != 0) return QB_EINVAL;
-  if (nbins < 1 || nbins > 65536) return QB_EINVAL;
-  if (N == 0) return QB_OK;
-  cudaStream_t s = as_stream(stream);
-  if (E == 256)
-    st = dtype == QB_F32 ? launch_route256_alpha_f32(logits, bias, N, k, alpha_out, s)
-                         : launch_route256_alpha_bf16(logits, bias, N, k, alpha_out, s);
-  else
-    st = launch_route_k3(logits, dtype, bias, N, E, k, nullptr, nullptr, nullptr, alpha_out,
-                         nullptr, bounds, nbins, s);
-  if (st != QB_OK) return st;
-  return launch_k3_count(logits, dtype, alpha_out, N, E, bounds, nbins, hist, s);
+  return k3_route_hist_impl(logits, dtype, bias, N, E, k, bounds, nbins, hist, alpha_out, stream,
+                            false);
+}
+
+int k3_route_hist_next(const void* logits, int dtype, const float* bias, int64_t N, int E,
+                       int k, const float* bounds, int nbins, int32_t* hist, float* alpha_out,
+                       void* stream) {
+  return k3_route_hist_impl(logits, dtype, bias, N, E, k, bounds, nbins, hist, alpha_out, stream,
+                            true);
 }
 
 int k3_finalize(int32_t* hist, int E, int nbins, int64_t r, float* bounds, float* bias_out,

@@ -45,11 +45,13 @@ int launch_route256_hi_f32(const void* logits, const float* bias, int64_t N, int
 int launch_route256_hi_bf16(const void* logits, const float* bias, int64_t N, int k,
                             int32_t* hist, uint16_t* keys_out, int32_t* topk_out,
                             float* alpha_out, cudaStream_t stream, bool chained = false);
-// alpha per token only (the first half of the K3 pass), E = 256.
+// alpha per token only (the first half of the K3 pass), E = 256; chained: a
+// further microbatch right after another K3 call on the stream
+// (k3_route_hist_next).
 int launch_route256_alpha_f32(const void* logits, const float* bias, int64_t N, int k,
-                              float* alpha_out, cudaStream_t stream);
+                              float* alpha_out, cudaStream_t stream, bool chained = false);
 int launch_route256_alpha_bf16(const void* logits, const float* bias, int64_t N, int k,
-                               float* alpha_out, cudaStream_t stream);
+                               float* alpha_out, cudaStream_t stream, bool chained = false);
 int launch_keys_hist_lo(const uint16_t* keys, int64_t N, int E, const int32_t* sel,
                         int32_t* hist_lo, cudaStream_t stream);
 int launch_select_hi(const int32_t* hist_hi, int E, int64_t r, int32_t* sel, int32_t* r_lo,

@@ -103,8 +103,12 @@ __global__ void __launch_bounds__(kCountThreads, 1)
   }
   // Launched as a programmatic dependent of the alpha pass: this CTA may have
   // cleared its counters while that pass still ran; wait for it (and its
-  // memory) before the first global read.
+  // memory) before the first global read.  Then the next microbatch's alpha
+  // pass, if chained (k3_route_hist_next), may start on the SMs this grid
+  // leaves: it writes another alpha buffer and reads nothing this kernel
+  // writes.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const float lo = ld_after_wait(bounds);
   const float hi = ld_after_wait(bounds + 1);
   const float scale = __fdiv_rn((float)nbins, __fsub_rn(hi, lo));

@@ -879,9 +879,10 @@ int launch_hi_t(const void* logits, const float* bias, int64_t N, int k, int32_t
 // alpha per token only (phases A and B), for the K3 counting kernel.
 template <typename T>
 int launch_alpha_t(const void* logits, const float* bias, int64_t N, int k, float* alpha_out,
-                   cudaStream_t stream) {
+                   cudaStream_t stream, bool chained = false) {
   Args a{logits, bias, N, k, nullptr, nullptr, nullptr, alpha_out, nullptr, nullptr, 0,
          device_status_ptr(), kE};
+  a.chained = chained ? 1 : 0;
   if (!a.status) return QB_ECUDA;
   return dispatch_k<T, kAlpha256>(k, a, stream);
 }

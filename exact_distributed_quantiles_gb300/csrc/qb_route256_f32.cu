@@ -10,7 +10,7 @@ int launch_route256_hi_f32(const void* logits, const float* bias, int64_t N, int
                                   chained);
 }
 int launch_route256_alpha_f32(const void* logits, const float* bias, int64_t N, int k,
-                               float* alpha_out, cudaStream_t stream) {
-  return r256::launch_alpha_t<float>(logits, bias, N, k, alpha_out, stream);
+                               float* alpha_out, cudaStream_t stream, bool chained) {
+  return r256::launch_alpha_t<float>(logits, bias, N, k, alpha_out, stream, chained);
 }
 }  // namespace qb

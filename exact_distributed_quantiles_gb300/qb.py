@@ -23,7 +23,8 @@ EXPORTS = ("qb_status_string", "qb_version", "qb_rank", "qb_sigmoid", "qb_sigmoi
            "qb_zero_i32",
            "qb_route_hist_hi", "qb_route_hist_hi_next", "qb_select_hi", "qb_keys_hist_lo",
            "qb_route_hist_lo",
-           "qb_finalize", "k3_route_hist", "k3_finalize", "lei_inject", "qb_device_status",
+           "qb_finalize", "k3_route_hist", "k3_route_hist_next", "k3_finalize", "lei_inject",
+           "qb_device_status",
            "lei_inject_noalloc", "qb_router_gemm", "qb_router_gemm_hist_hi",
            "qb_router_gemm_hist_hi_next", "qb_rank_average",
            "qb_maxvio", "lei_rho", "lei_apply",
@@ -56,6 +57,7 @@ def _load():
         "qb_route_hist_lo": (I, [P, I, P, I64, I, I, P, P, P]),
         "qb_finalize": (I, [P, P, P, P, I, P, P, I, P]),
         "k3_route_hist": (I, [P, I, P, I64, I, I, P, I, P, P, P]),
+        "k3_route_hist_next": (I, [P, I, P, I64, I, I, P, I, P, P, P]),
         "k3_finalize": (I, [P, I, I, I64, P, P, I, P]),
         "lei_inject": (I, [P, P, I64, I, I, F, I64, P, P]),
         "qb_device_status": (I, [ctypes.POINTER(ctypes.c_int)]),
@@ -186,6 +188,15 @@ def k3_route_hist(logits, bias, k, bounds, hist, alpha_out, stream=None):
     _check("k3_route_hist",
            lib.k3_route_hist(_ptr(logits), _dtype(logits), _ptr(bias), N, E, int(k), _ptr(bounds),
                              nbins, _ptr(hist), _ptr(alpha_out), _stream(stream)))
+
+
+def k3_route_hist_next(logits, bias, k, bounds, hist, alpha_out, stream=None):
+    N, E = logits.shape
+    nbins = hist.shape[1]
+    _check("k3_route_hist_next",
+           lib.k3_route_hist_next(_ptr(logits), _dtype(logits), _ptr(bias), N, E, int(k),
+                                  _ptr(bounds), nbins, _ptr(hist), _ptr(alpha_out),
+                                  _stream(stream)))
 
 
 def k3_finalize(hist, r, bounds, bias_out, reset=True, stream=None):

@@ -181,6 +181,18 @@ int k3_route_hist(const void* logits, int dtype, const float* bias, int64_t N, i
                   const float* bounds, int nbins, int32_t* hist, float* alpha_out,
                   void* stream);
 
+/* A further microbatch of the same global batch: the same operation and
+ * arguments as k3_route_hist, for a call issued on `stream` directly after a
+ * k3_route_hist or k3_route_hist_next call of the same batch (same bias,
+ * bounds and hist).  At E = 256 its alpha pass may start on the SMs that the
+ * previous call's counting leaves, so alpha_out must not be the previous
+ * call's alpha_out (two buffers used in turn suffice: the call before that
+ * has finished).  Ownership and ordering otherwise as qb_route_hist_hi_next.
+ * Other E: the same as k3_route_hist. */
+int k3_route_hist_next(const void* logits, int dtype, const float* bias, int64_t N, int E,
+                       int k, const float* bounds, int nbins, int32_t* hist, float* alpha_out,
+                       void* stream);
+
 /* K3 quantile, centering and next bounds ([QB-PR] "Quantile estimator"):
  *   b*  = first bin with cumulative count >= r, before = count below it,
  *   q_j = (lo + b* * width) + width * ((r - before) / count[b*]) in fp64,

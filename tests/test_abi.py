@@ -92,12 +92,14 @@ def test_argument_errors_are_reported_before_launch(lib):
     # finalize
     assert L.qb_finalize(fake, fake, fake, fake, 256, N0, N0, 1, N0) == lib.QB_EINVAL
     assert L.qb_finalize(N0, fake, fake, fake, 256, fake, N0, 1, N0) == lib.QB_EINVAL
-    # K3
-    assert L.k3_route_hist(fake, 1, fake, 10, 256, 8, fake, 0, fake, fake, N0) == lib.QB_EINVAL
-    assert L.k3_route_hist(fake, 1, fake, 10, 256, 8, N0, 1000, fake, fake, N0) == lib.QB_EINVAL
-    assert L.k3_route_hist(fake, 1, fake, 10, 256, 8, fake, 1000, fake, N0, N0) == lib.QB_EINVAL
-    assert L.k3_route_hist(fake, 1, fake, 10, 256, 8, fake, 1000, fake,
-                           ctypes.c_void_p(65537), N0) == lib.QB_EINVAL  # alpha_out misaligned
+    # K3 (plain and chained entries)
+    for k3 in (L.k3_route_hist, L.k3_route_hist_next):
+        assert k3(fake, 1, fake, 10, 256, 8, fake, 0, fake, fake, N0) == lib.QB_EINVAL
+        assert k3(fake, 1, fake, 10, 256, 8, N0, 1000, fake, fake, N0) == lib.QB_EINVAL
+        assert k3(fake, 1, fake, 10, 256, 8, fake, 1000, fake, N0, N0) == lib.QB_EINVAL
+        assert k3(fake, 1, fake, 10, 256, 8, fake, 1000, fake,
+                  ctypes.c_void_p(65537), N0) == lib.QB_EINVAL  # alpha_out misaligned
+        assert k3(fake, 1, fake, 0, 256, 8, fake, 1000, fake, fake, N0) == lib.QB_OK
     assert L.k3_finalize(fake, 256, 1000, 0, fake, fake, 1, N0) == lib.QB_EINVAL
     assert L.k3_finalize(fake, 256, 70000, 5, fake, fake, 1, N0) == lib.QB_EINVAL
     # LEI

@@ -64,13 +64,16 @@ def test_sigmoid_bit_equal_on_every_binary32_input(qb, orc):
 
 # ------------------------------------------------------------------ K3
 
-def _k3_gpu(qb, mbs, bias, k, bounds0, nbins):
+def _k3_gpu(qb, mbs, bias, k, bounds0, nbins, chained=False):
+    # chained: the microbatches after the first through k3_route_hist_next,
+    # with two alpha buffers used in turn
     E = bias.shape[0]
     hist = torch.zeros(E, nbins, dtype=torch.int32, device="cuda")
     bounds = bounds0.clone().cuda()
-    alpha = torch.empty(max(m.shape[0] for m in mbs), dtype=torch.float32, device="cuda")
-    for m in mbs:
-        qb.k3_route_hist(m, bias, k, bounds, hist, alpha[:m.shape[0]])
+    alpha = torch.empty(2, max(m.shape[0] for m in mbs), dtype=torch.float32, device="cuda")
+    for i, m in enumerate(mbs):
+        route = qb.k3_route_hist_next if chained and i else qb.k3_route_hist
+        route(m, bias, k, bounds, hist, alpha[i % 2, :m.shape[0]])
     n_pool = sum(m.shape[0] for m in mbs)
     h = hist.clone()
     b_out = torch.empty_like(bias)
@@ -97,11 +100,12 @@ def _check_k3(res, ref, bounds0, nbins):
     assert np.all(err <= 2 * ulp + width * 2.0 ** -22)
 
 
-def test_k3_workload(qb, orc):
+@pytest.mark.parametrize("chained", [False, True])
+def test_k3_workload(qb, orc, chained):
     w = inputs.WORKLOADS["k3"]
     bias, mbs = inputs.router_layer(w, inputs.seed_for("k3"), device="cuda")
     b0 = inputs.k3_initial_bounds(bias)
-    res = _k3_gpu(qb, mbs, bias, w.k, b0, w.nbins)
+    res = _k3_gpu(qb, mbs, bias, w.k, b0, w.nbins, chained=chained)
     ref = orc.k3_global_batch([host_logits(m) for m in mbs], bias.cpu().numpy(), w.k,
                               b0.numpy(), w.nbins)
     _check_k3(res, ref, b0.numpy(), w.nbins)
@@ -122,7 +126,7 @@ def test_k3_small_shapes(qb, orc, E, k, nbins, dtype):
                       nbins=nbins, logits_dtype=dtype)
     bias, mbs = inputs.router_layer(w, 31 + E, device="cuda")
     b0 = inputs.k3_initial_bounds(bias)
-    res = _k3_gpu(qb, mbs, bias, w.k, b0, nbins)
+    res = _k3_gpu(qb, mbs, bias, w.k, b0, nbins, chained=E % 64 == 0)
     ref = orc.k3_global_batch([host_logits(m) for m in mbs], bias.cpu().numpy(), w.k,
                               b0.numpy(), nbins)
     _check_k3(res, ref, b0.numpy(), nbins)

@@ -42,17 +42,17 @@ METRIC = "QB routed tokens/s per layer (E=256,k=6, 2-pass EQB) on 1 GB300; % of 
 # launch (route256_kernel, keys written, no top-k output) on a 524288-token
 # layer, from an ncu capture of that launch.  Reported only while the
 # kernel's sources hash to the value they had when the counters were taken.
-ROUTE_TRAFFIC = {"sha1": "b37950200c38f8f6fa005644cd04527edcbf9200", "tokens": 524288,
-                 "bytes": (537.040896 + 232.976896) * 1e6}
+ROUTE_TRAFFIC = {"sha1": "9caf9b404b8e9a128ce7dfb04ff503deabad3269", "tokens": 524288,
+                 "bytes": (537.010432 + 232.794368) * 1e6}
 ROUTE_SOURCES = ("qb_route256.cuh", "qb_route256_f32.cu", "qb_route.cuh", "qb_device.cuh")
 # Warp instructions of the same capture (smsp__inst_executed.sum), for the
 # issue-rate roofline of this issue-bound kernel; same hash guard.
-ROUTE_INSTR = {"tokens": 524288, "warp_instructions": 127038039}
+ROUTE_INSTR = {"tokens": 524288, "warp_instructions": 126612727}
 # Warp instructions (smsp__inst_executed.sum) of one K3 microbatch of 65536
 # bf16 tokens: the alpha pass (route256_kernel, K3 mode) plus the count
 # kernel, from an ncu capture of those launches; reported while the K3
 # sources hash to the value they had when it was taken.
-K3_INSTR = {"sha1": "bf0cfb4e3b06c4db6a6ec80c73bba64f29a8be0b", "tokens": 65536,
+K3_INSTR = {"sha1": "afc61768ab95c5de323af2ba864056ba75218ff8", "tokens": 65536,
             "warp_instructions": 12850624 + 13207384}
 K3_SOURCES = ("qb_route256.cuh", "qb_route256_bf16.cu", "qb_route.cuh", "qb_device.cuh",
               "qb_k3.cu")

@@ -740,6 +740,7 @@ __global__ void __launch_bounds__(warps_max(MODE) * 32, 1) route256_kernel(const
     for (int q = 0; q < kPairs; ++q) issue_pair<T>(c, s0, rows0, q);
   }
   uint32_t parity = 0;
+  bool clean = true;  // no wait of this warp gave up
   for (; tix < n_tiles; tix += wstride) {
     const int64_t t0 = tix * kTile;
     const int rows = (int)((a.N - t0) < kTile ? (a.N - t0) : kTile);
@@ -749,14 +750,19 @@ __global__ void __launch_bounds__(warps_max(MODE) * 32, 1) route256_kernel(const
     const bool ok = rows == kTile
                         ? tile_pass<T, KL, K1, MODE, true>(c, breg, t0, rows, n0, nrows, parity)
                         : tile_pass<T, KL, K1, MODE, false>(c, breg, t0, rows, n0, nrows, parity);
-    if (!ok) break;
+    if (!ok) {
+      clean = false;
+      break;
+    }
     parity ^= 1u;
   }
 
-  // ---- flush the shared window
+  // ---- flush the shared window (after every warp's increments)
   if constexpr (MODE == kHi256) {
     const int nw = (int)(blockDim.x >> 5);
-    if ((reinterpret_cast<uintptr_t>(a.hist) & 15) == 0 && nw * kWarpBytes >= kE * kStg * 4) {
+    const bool all_clean = __syncthreads_and(clean ? 1 : 0) != 0;
+    if (all_clean && (reinterpret_cast<uintptr_t>(a.hist) & 15) == 0 &&
+        nw * kWarpBytes >= kE * kStg * 4) {
       // Through the (now idle) tile buffers: the window is copied into rows
       // r = 32 i + L (expert expert_of(L, i)) of kStg words, whose slots 0-15
       // and 16-31 are two runs of 16 consecutive counters of the expert's
@@ -765,9 +771,10 @@ __global__ void __launch_bounds__(warps_max(MODE) * 32, 1) route256_kernel(const
       // one atomic per counter).  Both copies are conflict-free: the reads
       // take 32 consecutive words, and the 16-byte writes of a quarter-warp
       // land on 8 different 16-byte bank groups ((9 r + q) % 8 differs).
-      // Every lane first waits for its own row copies (after a timed-out
-      // wait some may still be landing in those buffers) and the row-pair
-      // barriers living in the buffers are invalidated.
+      // Taken only when no wait of the CTA gave up, so no row copy or its
+      // barrier arrival is outstanding; every lane still waits for its own
+      // copies, and the row-pair barriers living in the buffers are
+      // invalidated before the buffers are reused.
       asm volatile("cp.async.wait_all;" ::: "memory");
       if (lane == 0)
         for (int q = 0; q < kPairs; ++q)
@@ -794,8 +801,9 @@ __global__ void __launch_bounds__(warps_max(MODE) * 32, 1) route256_kernel(const
       asm volatile("cp.async.bulk.commit_group;" ::: "memory");
       asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     } else {
-      // a histogram that is not 16-byte aligned: one atomic per non-zero counter
-      __syncthreads();
+      // a histogram that is not 16-byte aligned, or a wait that gave up (its
+      // copies may still land in the tile buffers): one atomic per non-zero
+      // counter, straight from the window
       for (int w = threadIdx.x; w < kWin * kE; w += blockDim.x) {
         const int cnt = hist_s[w];
         if (cnt) {
